@@ -1,0 +1,431 @@
+#!/usr/bin/env python3
+"""Throughput of lossless exponent-reuse compression + gather-decompress.
+
+One step = one training iteration of the workload's weights through the
+whole path: compress of all R simulated ranks (one launch) and the fused
+gather-decompress of all R payloads (bitmap scan + one launch), with both
+exponent caches carried from step to step.  Metric: bf16 weight GB/s =
+2*N bytes per step / time, and the same traffic as a fraction of the
+measured HBM copy bandwidth.
+
+Default workload: one OLMoE-shaped MoE layer (64 experts x {gate, up
+2048x1024, down 1024x2048}, 402,653,184 bf16 values, N(0, 0.02)), 16
+simulated ranks, block 4096, Adam-like step 1e-5 * N(0,1) per iteration.
+Inputs (805 MB per iteration) are larger than the 129 MB L2, so no flush is
+needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config 1..5] [--variant clustered0.1]
+
+Under torchrun (N > 1) each rank runs an independent replica of the
+workload on its own GPU (weak scaling; the path has no data exchange on one
+GPU), and rank 0 prints max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import csv
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "bf16 weight GB/s (compress + gather-decompress) and % of GB300 HBM peak"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--variant", default="")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# process group (replicas only: used for the barrier and the max over ranks)
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, x: float) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(world, x: float) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(f"/tmp/ciera_clocks_{os.getpid()}.csv", "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.out.name) as f:
+            for row in csv.reader(f):
+                if len(row) >= 9:
+                    rows.append([c.strip() for c in row])
+        os.unlink(self.out.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
+                          and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(descs, numel):
+    """(compress bytes, decompress bytes, changed fraction) of one step.
+
+    compress:   read w 2N + sender cache N, write payloads P + exponents of
+                changed values C            = 3N + P + C
+    decompress: read payloads P + cached exponents of kept values N - C,
+                write out 2N + exponents of changed values C = 3N + P
+    A raw payload counts all its values as changed; a compressed body holds
+    len + (values in changed blocks) bytes.
+    """
+    P = sum(d["payload_bytes"] for d in descs)
+    raw_vals = sum(d["payload_bytes"] // 2 for d in descs if d["mode"] == 1)
+    comp_vals = numel - raw_vals
+    comp_changed = sum(d["body_bytes"] for d in descs if d["mode"] == 0) - comp_vals
+    C = raw_vals + comp_changed
+    return 3 * numel + P + C, 3 * numel + P, C / max(numel, 1)
+
+
+def gen_sequence(wl, iterations, device, layer=0):
+    from lossless_exponent_reuse_gb300 import workloads
+    seq = [workloads.initial_layer(wl, layer, device)]
+    for t in range(1, iterations):
+        seq.append(workloads.step_layer(wl, seq[-1], layer, t))
+    return seq
+
+
+def cpu_baseline(wl, seq_host, warm_t, budget_s):
+    """Time the oracle (as it stands) on the host cores over a bounded sample:
+    iteration warm_t of a subset of ranks, each rank's caches prepared by an
+    untimed oracle pass over iteration warm_t - 1."""
+    import oracle
+    n, R, B = seq_host[0].size, wl.ranks, wl.block
+    threads = min(os.cpu_count() or 1, R)
+    prev, cur = seq_host[warm_t - 1], seq_host[warm_t]
+
+    def prep(r):
+        b, ln = oracle.shard_begin(n, R, r), oracle.shard_len(n, R, r)
+        sc = np.zeros(ln, np.uint8)
+        rc = np.zeros(ln, np.uint8)
+        p, _, d = oracle.compress_shard(prev[b:b + ln], B, sc, True)
+        oracle.decompress_shard(p, d, ln, B, rc)
+        return r, b, ln, sc, rc
+
+    def run(item):
+        r, b, ln, sc, rc = item
+        p, _, d = oracle.compress_shard(cur[b:b + ln], B, sc, False)
+        st, _ = oracle.decompress_shard(p, d, ln, B, rc)
+        assert st == 0
+        return ln
+
+    # size the sample: one rank first, then as many as fit the budget
+    with cf.ThreadPoolExecutor(threads) as ex:
+        first = prep(0)
+        t0 = time.perf_counter()
+        run(first)
+        one = time.perf_counter() - t0
+        ranks = max(1, min(R, int(budget_s * threads / max(one, 1e-6))))
+        ranks = max(threads, ranks) if R >= threads else R
+        ranks = min(R, ranks)
+        items = list(ex.map(prep, range(ranks)))
+        t0 = time.perf_counter()
+        done = sum(ex.map(run, items))
+        dt = time.perf_counter() - t0
+    return {"value": 2.0 * done / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"iteration {warm_t} of {ranks}/{R} ranks ({done} values), "
+                      f"compress+decompress, one rank per thread"}
+
+
+def run_ours(args, world, rank, local):
+    from lossless_exponent_reuse_gb300 import ciera, workloads
+    from lossless_exponent_reuse_gb300.allgather import SimulatedAllgather
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = workloads.workload(args.config, args.variant)
+    if wl.layers != 1:
+        raise SystemExit("bench.py times single-layer workloads (configs 1, 2, 3, 5)")
+    W, K = args.warmup, args.steps
+    iters = W + K
+    n = wl.layer_numel
+    seq = gen_sequence(wl, iters, dev)
+    torch.cuda.synchronize()
+
+    ag = SimulatedAllgather(n, wl.block, wl.ranks, device=dev)
+    stream = torch.cuda.current_stream()
+    for t in range(W):
+        ag.step(seq[t])
+    if ag.status() != ciera.OK:
+        raise RuntimeError("warm-up reported an error status")
+    snap_s, snap_r = ag.sender_cache.clone(), ag.recv_cache.clone()
+    it0 = ag.iteration
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        ag.compress(seq[W + i])
+        ev[i][1].record(stream)
+        ag.decompress()
+        ev[i][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    if ag.status() != ciera.OK:
+        raise RuntimeError("timed steps reported an error status")
+    total_ms = start.elapsed_time(end)
+    t_c = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    t_d = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    final_out = ag.out.view(torch.int16).clone()
+    final_s, final_r = ag.sender_cache.clone(), ag.recv_cache.clone()
+
+    # untimed replay from the same state: per-step descriptors for the byte
+    # accounting, and a determinism check against the timed run
+    ag.sender_cache.copy_(snap_s)
+    ag.recv_cache.copy_(snap_r)
+    ag.iteration = it0
+    bytes_c, bytes_d, fvals = [], [], []
+    for i in range(K):
+        ag.compress(seq[W + i])
+        bc, bd, f = algorithmic_bytes(ag.descriptors(), n)
+        bytes_c.append(bc)
+        bytes_d.append(bd)
+        fvals.append(f)
+        ag.decompress()
+    torch.cuda.synchronize()
+    if not (torch.equal(final_out, ag.out.view(torch.int16)) and torch.equal(final_s, ag.sender_cache)
+            and torch.equal(final_r, ag.recv_cache)):
+        raise RuntimeError("replay differs from the timed run")
+    if not torch.equal(ag.out[:n].view(torch.int16), seq[W + K - 1].view(torch.int16)):
+        raise RuntimeError("round trip is not exact")
+
+    peak, peak_kind = measured_peak()
+    total_s = max_over_ranks(world, total_ms / 1e3)
+    values = sum_over_ranks(world, float(n * K))
+    value = 2.0 * values / total_s / 1e9
+    hbm_gbs = sum_over_ranks(world, float(sum(bytes_c) + sum(bytes_d))) / total_s / 1e9
+    mc, md = statistics.mean(t_c), statistics.mean(t_d)
+    if mc >= md:
+        dom, dom_bytes, dom_ms = "k_compress", statistics.mean(bytes_c), mc
+    else:
+        dom, dom_bytes, dom_ms = "k_bitmap_scan+k_decompress", statistics.mean(bytes_d), md
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(total_s * 1e3 / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "numel": n, "ranks": wl.ranks, "block": wl.block,
+                   "step": wl.steps[0], "iterations_timed": f"{W}..{W + K - 1}",
+                   "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (805 MB of weights per step), no flush"},
+        "hbm": {"achieved_gbs": round(hbm_gbs, 1), "peak_gbs": peak,
+                "frac": round(hbm_gbs / peak, 4), "peak_kind": peak_kind,
+                "changed_fraction": round(statistics.mean(fvals), 4)},
+        "kernels_ms": {"compress": round(mc, 4), "decompress": round(md, 4)},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None, "peak_kind": peak_kind},
+        "gpu_launches": K * 3,
+        "clocks": clk,
+    }
+
+    del ag
+    torch.cuda.empty_cache()
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(wl, seq, W, K, dev, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        seq_host = [s.view(torch.int16).cpu().numpy().view(np.uint16) for s in seq[:W + 1]]
+        result["cpu_baseline"] = cpu_baseline(wl, seq_host, W, args.cpu_seconds)
+    return result
+
+
+def run_e2e(wl, seq, W, K, dev, world):
+    """The same metric through host buffers: each step copies its weights
+    from pinned host memory, runs the path and reads the result back."""
+    from lossless_exponent_reuse_gb300 import ciera
+    from lossless_exponent_reuse_gb300.allgather import SimulatedAllgather
+    n = wl.layer_numel
+    host = [s.view(torch.int16).to("cpu").pin_memory() for s in seq]
+    out_host = torch.empty(n, dtype=torch.int16).pin_memory()
+    w_dev = torch.empty(n, dtype=torch.int16, device=dev)
+    ag = SimulatedAllgather(n, wl.block, wl.ranks, device=dev)
+    stream = torch.cuda.current_stream()
+    for t in range(W):
+        ag.step_host(host[t], out_host, w_dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(K):
+        ag.step_host(host[W + i], out_host, w_dev)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    if ag.status() != ciera.OK:
+        raise RuntimeError("e2e steps reported an error status")
+    if not torch.equal(out_host.view(torch.int16), host[W + K - 1].view(torch.int16)):
+        raise RuntimeError("e2e round trip is not exact")
+    t = max_over_ranks(world, start.elapsed_time(end) / 1e3)
+    val = 2.0 * sum_over_ranks(world, float(n * K)) / t / 1e9
+    return {"value": round(val, 2), "unit": UNIT, "h2d_bytes_per_step": 2 * n,
+            "d2h_bytes_per_step": 2 * n}
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: on the host cores, bounded samples."""
+    if rank != 0:
+        return None
+    from lossless_exponent_reuse_gb300 import workloads
+    import oracle
+    wl = workloads.workload(args.config, args.variant)
+    n, R, B = wl.layer_numel, wl.ranks, wl.block
+    W, K = args.warmup, args.steps
+    # each step: one rank's shard of one iteration, compress + decompress
+    S = oracle.shard_size(n, R)
+    seq = gen_sequence(wl, W + K + 1, "cpu")
+    seq_host = [s.numpy() for s in seq]
+    threads = 1
+    sc = np.zeros(S, np.uint8)
+    rc = np.zeros(S, np.uint8)
+    p, _, d = oracle.compress_shard(seq_host[0][:S], B, sc, True)
+    oracle.decompress_shard(p, d, S, B, rc)
+    for t in range(1, W + 1):
+        p, _, d = oracle.compress_shard(seq_host[t][:S], B, sc, False)
+        oracle.decompress_shard(p, d, S, B, rc)
+    t0 = time.perf_counter()
+    for i in range(K):
+        p, _, d = oracle.compress_shard(seq_host[W + 1 + i][:S], B, sc, False)
+        st, _ = oracle.decompress_shard(p, d, S, B, rc)
+        assert st == 0
+    dt = time.perf_counter() - t0
+    val = 2.0 * S * K / dt / 1e9
+    return {"metric": METRIC, "value": round(val, 4), "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": round(dt * 1e3 / K, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": wl.name, "numel": n, "ranks": R, "block": B,
+                       "sample": f"rank 0 shard ({S} values) per step"},
+            "cpu_baseline": {"value": round(val, 4), "unit": UNIT, "cores": threads,
+                             "kind": "oracle",
+                             "sample": f"rank 0 shard of iterations {W + 1}..{W + K}, "
+                                       f"compress+decompress"},
+            "e2e": {"value": round(val, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_ours(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

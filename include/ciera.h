@@ -1,0 +1,192 @@
+/*
+ * ciera.h -- C ABI of libciera: lossless cross-iteration exponent reuse for
+ * sharded bf16 weights, on one GB300 (sm_103a).
+ *
+ * Method: "CIERA: Cross-Iteration Exponent Reuse for Lossless Allgather in
+ * Sharded MoE Training" (Sadiq, Shen, Tanaka).  Section 3.1 (Exponent Reuse)
+ * splits each bf16 value into its 8-bit exponent and a sign+mantissa byte,
+ * detects per block whether any exponent changed since the previous
+ * iteration, and sends only sign+mantissa for unchanged blocks; the receiver
+ * rebuilds each value from its cached exponent (Appendix A, Algorithm 1).
+ * Section 3.2 (Benefit-driven Selective Compression) decides per tensor
+ * whether compressing pays.
+ *
+ * Model of the data-parallel path.  A flat buffer of N bf16 values is split
+ * into R contiguous shards of S = ceil(N/R) values (the last may be short or
+ * empty); rank r owns [r*S, min((r+1)*S, N)).  Each shard is cut into blocks
+ * of B values (the last block of a shard may be partial).  A sender turns its
+ * shard into one payload; a receiver turns all R payloads (the Allgather
+ * result: rank r's payload at payloads + r*stride) back into the N values.
+ *
+ * Payload of one shard (len values, n_b = ceil(len/B) blocks):
+ *   COMPRESSED  body || bitmap.  The body holds the blocks in order; an
+ *               unchanged block contributes its len_k sign+mantissa bytes
+ *               (sign in bit 7, mantissa in bits 0..6), a changed block its
+ *               len_k bf16 values (2*len_k bytes, little-endian).  The bitmap
+ *               has ceil(n_b/8) bytes; block k is bit (k%8) of byte k/8,
+ *               padding bits are zero.
+ *   RAW         the shard's 2*len bf16 bytes verbatim, no bitmap.  Chosen on
+ *               a cold start, for an empty shard, or when body + bitmap would
+ *               not be smaller than 2*len.  With every block changed the
+ *               compressed body equals the raw bytes, so "all changed falls
+ *               back to raw".
+ * A block is changed iff any of its exponents differs from the sender's
+ * cached exponent (an exact compare).  A cold start marks every block
+ * changed.
+ *
+ * Conventions for every call:
+ *   - Return value: CIERA_OK (0) or a negative CIERA_E_* code; no exceptions
+ *     cross the ABI.  Errors found by a kernel (a corrupt descriptor on the
+ *     receiver, a bounded wait that ran out) are recorded in a status word in
+ *     the workspace and returned by ciera_status().
+ *   - All device pointers are owned by the caller; the library allocates no
+ *     device memory.  A plan owns only host metadata.
+ *   - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t;
+ *     NULL means the legacy default stream).  They run on the current device.
+ *   - A workspace must be zero-filled once before its first use (or passed to
+ *     ciera_workspace_init) and must not be used by two calls that can run at
+ *     the same time.
+ *   - Fast path: when B is a multiple of 16 in [256, 16384], S is a multiple
+ *     of 16, every pointer is 16-byte aligned and the payload stride is a
+ *     multiple of 16, blocks are staged through shared memory with bulk
+ *     copies; otherwise a byte-wise path gives the same bytes.
+ */
+#ifndef CIERA_H
+#define CIERA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CIERA_OK 0
+#define CIERA_E_INVAL (-1)       /* bad argument (size, pointer, alignment, range) */
+#define CIERA_E_CUDA (-2)        /* a CUDA runtime call failed */
+#define CIERA_E_CORRUPT (-3)     /* a received descriptor/bitmap does not match the plan */
+#define CIERA_E_TIMEOUT (-4)     /* a bounded device-side wait ran out */
+
+#define CIERA_MODE_COMPRESSED 0u
+#define CIERA_MODE_RAW 1u
+
+/* ciera_compress flags */
+#define CIERA_COLD 1u            /* no previous exponents: every block changed, payload raw */
+/* Test hook: the first tile of every shard never publishes its prefix, so
+ * that the tiles after it run into the bounded wait (CIERA_E_TIMEOUT). */
+#define CIERA_DEBUG_SKIP_FIRST_PUBLISH 0x80000000u
+
+typedef struct ciera_plan_s *ciera_plan_t;
+
+/* Descriptor of one rank's payload, device-resident, 24 bytes. */
+typedef struct {
+    uint32_t mode;             /* CIERA_MODE_COMPRESSED or CIERA_MODE_RAW */
+    uint32_t n_changed_blocks; /* blocks whose exponents changed (all on a cold start) */
+    uint64_t body_bytes;       /* bytes before the bitmap (2*len when raw) */
+    uint64_t payload_bytes;    /* total bytes to send (body + bitmap, or 2*len) */
+} ciera_desc;
+
+/* Host-side facts of a plan. */
+typedef struct {
+    int64_t numel;             /* N */
+    int64_t ranks;             /* R */
+    int64_t block;             /* B */
+    int64_t shard_len;         /* S = ceil(N/R) */
+    int64_t blocks_per_shard;  /* ceil(S/B): per-rank stride of the flags output */
+    int64_t tile_blocks;       /* blocks handled by one CTA */
+    int64_t total_tiles;       /* CTAs of a full-range compress or decompress */
+    int64_t payload_capacity;  /* minimum payload stride: 2*S rounded up to 256 bytes */
+    int64_t workspace_bytes;   /* bytes of device workspace a call needs */
+    int32_t fast_path;         /* 1 if sizes allow the shared-memory staged path */
+    int32_t raw_fixup;         /* 1 if a raw payload can hold unchanged blocks (tiny B) */
+} ciera_plan_info_t;
+
+/* Cost model of the per-tensor predicate (Section 3.2, gain g_i). */
+typedef struct {
+    double link_Bps;           /* Allgather bandwidth the payload saves, bytes/s */
+    double q_hat;              /* expected fraction of values in changed blocks */
+    double t_fixed_s;          /* fixed per-tensor cost: launches, size exchange */
+    double hbm_Bps;            /* receiver memory bandwidth, bytes/s */
+    int64_t block;             /* block size B used for the bitmap term */
+} ciera_cost_model;
+
+/* Build a plan for a tensor of `ndim` dims `shape` (flattened, row-major),
+ * block size `block` >= 1, `ranks` >= 1 simulated ranks.  Section 3.1 (block
+ * partition inside each shard) and Section 3.2 (S_b = ceil(N/B)).
+ * Errors: CIERA_E_INVAL for ndim < 0, a negative dim, block < 1, ranks < 1,
+ * N >= 2^40, or more than 2^30 blocks per shard.  *out is set only on
+ * success; free it with ciera_plan_destroy. */
+int ciera_plan(const int64_t *shape, int ndim, int64_t block, int ranks, ciera_plan_t *out);
+
+/* Fill *info.  Errors: CIERA_E_INVAL for a NULL argument. */
+int ciera_plan_info(ciera_plan_t plan, ciera_plan_info_t *info);
+
+/* Free a plan (NULL is ignored). */
+void ciera_plan_destroy(ciera_plan_t plan);
+
+/* Zero-fill a workspace of info.workspace_bytes bytes on `stream`. */
+int ciera_workspace_init(ciera_plan_t plan, void *workspace_dev, void *stream);
+
+/* Sender side (Section 3.1; Algorithm 1, sender) for ranks
+ * [rank_begin, rank_begin + rank_count), all in one launch.
+ *   w_dev            bf16 bit patterns of those ranks' shards, contiguous:
+ *                    element 0 is the first element of shard rank_begin
+ *                    (the whole tensor when rank_begin == 0 and all ranks)
+ *   sender_cache_dev one exponent byte per element of the same range: the
+ *                    exponents sent last iteration; updated in place
+ *   payloads_dev     rank_count payload slots, slot i at
+ *                    payloads_dev + i*payload_stride (>= payload_capacity)
+ *   descs_dev        rank_count descriptors (device memory)
+ *   flags_dev        optional (may be NULL): rank_count rows of
+ *                    blocks_per_shard bytes, 1 = block changed
+ *   workspace_dev    info.workspace_bytes bytes, see the conventions above
+ *   flags            CIERA_COLD, or 0
+ * Errors: CIERA_E_INVAL for a bad range, NULL pointer or short stride;
+ * CIERA_E_CUDA if a launch fails.  CIERA_E_TIMEOUT appears later through
+ * ciera_status(). */
+int ciera_compress(ciera_plan_t plan, int rank_begin, int rank_count, const uint16_t *w_dev,
+                   uint8_t *sender_cache_dev, uint8_t *payloads_dev, int64_t payload_stride,
+                   ciera_desc *descs_dev, uint8_t *flags_dev, void *workspace_dev, uint32_t flags,
+                   void *stream);
+
+/* Receiver side (Section 3.1; Algorithm 1, receiver): rebuilds all N values
+ * from the R payloads and refreshes the receiver's exponent cache.
+ *   payloads_dev   R payloads, rank r's at payloads_dev + r*payload_stride
+ *   descs_dev      R descriptors (device memory)
+ *   recv_cache_dev N exponent bytes (ExpCache); updated in place
+ *   out_dev        N bf16 outputs
+ * A rank whose descriptor or bitmap does not match the plan is skipped (its
+ * output range is left untouched) and CIERA_E_CORRUPT is recorded for
+ * ciera_status().  Errors: CIERA_E_INVAL, CIERA_E_CUDA. */
+int ciera_decompress(ciera_plan_t plan, const uint8_t *payloads_dev, int64_t payload_stride,
+                     const ciera_desc *descs_dev, uint8_t *recv_cache_dev, uint16_t *out_dev,
+                     void *workspace_dev, uint32_t flags, void *stream);
+
+/* Wait for `stream`, then read and clear the workspace's status word.
+ * Returns CIERA_OK, CIERA_E_CORRUPT, CIERA_E_TIMEOUT or CIERA_E_CUDA. */
+int ciera_status(void *workspace_dev, void *stream);
+
+/* Per-tensor predicate (Section 3.2): 1 = compress, 0 = send raw.
+ * With P = N + q*N + ceil(ceil(N/B)/8) expected payload bytes,
+ * compress iff (2N - P)/link_Bps > t_fixed_s + (4 + q)*N/hbm_Bps. */
+int ciera_should_compress(int64_t numel);
+
+/* Replace / read the process-wide cost model.  Defaults: link 8e9 B/s,
+ * q_hat 0.22, t_fixed 20e-6 s, hbm 8e12 B/s, block 4096.
+ * Errors: CIERA_E_INVAL for NULL, non-positive rates, q_hat outside [0,1],
+ * negative t_fixed or block < 1. */
+int ciera_set_cost_model(const ciera_cost_model *model);
+int ciera_get_cost_model(ciera_cost_model *model);
+
+/* Limit of every bounded device-side wait, in nanoseconds (default 1 s).
+ * Errors: CIERA_E_INVAL for 0. */
+int ciera_set_wait_timeout_ns(uint64_t ns);
+
+/* Static description of a status code. */
+const char *ciera_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CIERA_H */

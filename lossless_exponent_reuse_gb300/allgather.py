@@ -1,0 +1,69 @@
+"""One exponent-reuse Allgather of a flat bf16 buffer, R simulated ranks on one GPU.
+
+The R senders' payloads are laid out in this GPU's memory exactly as an
+Allgather would deliver them (rank r's payload at row r), so the receiver
+side runs on the real gathered layout; no collective is involved.
+
+CIERA ("Cross-Iteration Exponent Reuse for Lossless Allgather in Sharded MoE
+Training"), Section 3.1: every sender keeps the exponents it sent last
+iteration, every receiver keeps the exponents of every shard (ExpCache);
+both caches persist across iterations.  The first call is a cold start.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import ciera
+
+
+class SimulatedAllgather:
+    """Device state of one plan: both exponent caches, payloads, descriptors."""
+
+    def __init__(self, numel: int, block: int, ranks: int, device="cuda",
+                 keep_flags: bool = False):
+        self.plan = ciera.Plan(numel, block, ranks)
+        info = self.plan.info
+        self.numel = numel
+        self.device = torch.device(device)
+        self.sender_cache = torch.zeros(max(numel, 1), dtype=torch.uint8, device=device)
+        self.recv_cache = torch.zeros(max(numel, 1), dtype=torch.uint8, device=device)
+        self.payloads = self.plan.new_payloads(device=device)
+        self.descs = self.plan.new_descs(device=device)
+        self.workspace = self.plan.new_workspace(device=device)
+        self.flags = (torch.zeros((ranks, max(info.blocks_per_shard, 1)), dtype=torch.uint8,
+                                  device=device) if keep_flags else None)
+        self.out = torch.empty(max(numel, 1), dtype=torch.uint16, device=device)
+        self.iteration = 0
+
+    def compress(self, w: torch.Tensor, stream=None) -> None:
+        self.plan.compress(w, self.sender_cache, self.payloads, self.descs, self.workspace,
+                           cold=self.iteration == 0, flags_out=self.flags, stream=stream)
+
+    def decompress(self, stream=None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        o = self.out if out is None else out
+        self.plan.decompress(self.payloads, self.descs, self.recv_cache, o, self.workspace,
+                             stream=stream)
+        self.iteration += 1
+        return o
+
+    def step(self, w: torch.Tensor, stream=None) -> torch.Tensor:
+        """Sender side for all ranks, then the fused gather-decompress."""
+        self.compress(w, stream=stream)
+        return self.decompress(stream=stream)
+
+    def step_host(self, w_host: torch.Tensor, out_host: torch.Tensor, w_dev: torch.Tensor,
+                  stream=None) -> None:
+        """End-to-end from host memory: copy this iteration's weights in,
+        run the path, copy the rebuilt weights out (pinned buffers)."""
+        w_dev.view(torch.int16).copy_(w_host.view(torch.int16), non_blocking=True)
+        self.step(w_dev, stream=stream)
+        out_host.view(torch.int16).copy_(self.out[: self.numel].view(torch.int16),
+                                         non_blocking=True)
+
+    def status(self, stream=None) -> int:
+        return ciera.status(self.workspace, stream=stream)
+
+    def descriptors(self):
+        return ciera.decode_descs(self.descs)

@@ -1,0 +1,297 @@
+// ciera_api.cpp -- host side of the libciera C ABI: plans, argument checks,
+// workspace layout, the per-tensor predicate and status reporting.
+//
+// Method: "CIERA: Cross-Iteration Exponent Reuse for Lossless Allgather in
+// Sharded MoE Training", Section 3.1 (block partition of each shard) and
+// Section 3.2 (block count, bitmap size, gain of a shard).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include <new>
+
+#include "ciera.h"
+#include "ciera_internal.h"
+
+using namespace ciera;
+
+struct ciera_plan_s {
+  int64_t numel;
+  int64_t ranks;
+  int64_t block;
+  int64_t S;           // shard size
+  int64_t nb_full;     // blocks of a full shard
+  int64_t T;           // blocks per tile
+  int64_t tiles_full;
+  int64_t r_full;      // shards of exactly S values
+  int64_t len_part;    // values of the one partial shard (0 if none)
+  int64_t tiles_part;
+  int64_t total_tiles;
+  int64_t capacity;
+  int64_t flag_stride;
+  int64_t nw_stride;
+  int64_t off_status, off_flags, off_words, off_prefix, off_rstate, ws_bytes;
+  int64_t smem_bytes;  // dynamic shared memory of the staged path
+  bool fast;
+  bool raw_fixup;
+};
+
+namespace {
+
+std::atomic<uint32_t> g_epoch{0};
+std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+std::mutex g_cost_mu;
+ciera_cost_model g_cost = {8e9, 0.22, 20e-6, 8e12, 4096};
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t align_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+uint32_t next_epoch() {
+  uint32_t e;
+  do {
+    e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  } while (e == 0);  // a zero-filled workspace holds epoch 0: never valid
+  return e;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Geometry of ranks [rb, rb+rc).
+Geometry range_geometry(const ciera_plan_s* p, int64_t rb, int64_t rc) {
+  Geometry g{};
+  g.S = p->S;
+  g.B = p->block;
+  g.T = p->T;
+  g.tiles_full = p->tiles_full;
+  int64_t nfull = p->r_full - rb;
+  if (nfull < 0) nfull = 0;
+  if (nfull > rc) nfull = rc;
+  const bool has_part = p->len_part > 0 && rb <= p->r_full && p->r_full < rb + rc;
+  g.nfull = static_cast<int32_t>(nfull);
+  g.has_part = has_part ? 1 : 0;
+  g.len_part = has_part ? p->len_part : 0;
+  g.tiles_part = has_part ? p->tiles_part : 0;
+  g.rank_count = static_cast<int32_t>(rc);
+  g.total_tiles = nfull * p->tiles_full + g.tiles_part;
+  return g;
+}
+
+// Smallest block of a shard of `len` values: a raw payload can hold an
+// unchanged block only if some block is not larger than the bitmap.
+bool raw_can_hold_unchanged(int64_t len, int64_t B) {
+  if (len <= 0) return false;
+  const int64_t nb = ceil_div(len, B);
+  const int64_t last = len - (nb - 1) * B;
+  const int64_t smallest = last < B ? last : B;
+  return smallest <= ceil_div(nb, 8);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ciera_strerror(int status) {
+  switch (status) {
+    case CIERA_OK: return "ok";
+    case CIERA_E_INVAL: return "invalid argument";
+    case CIERA_E_CUDA: return "CUDA runtime error";
+    case CIERA_E_CORRUPT: return "corrupt descriptor or bitmap";
+    case CIERA_E_TIMEOUT: return "bounded device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int ciera_plan(const int64_t* shape, int ndim, int64_t block, int ranks, ciera_plan_t* out) {
+  if (!out || ndim < 0 || (ndim > 0 && !shape) || block < 1 || ranks < 1) return CIERA_E_INVAL;
+  int64_t n = 1;
+  for (int i = 0; i < ndim; ++i) {
+    if (shape[i] < 0) return CIERA_E_INVAL;
+    if (shape[i] != 0 && n > kMaxNumel / shape[i]) return CIERA_E_INVAL;
+    n *= shape[i];
+  }
+  if (n >= kMaxNumel) return CIERA_E_INVAL;
+  ciera_plan_s* p = new (std::nothrow) ciera_plan_s();
+  if (!p) return CIERA_E_INVAL;
+  p->numel = n;
+  p->ranks = ranks;
+  p->block = block;
+  p->S = n > 0 ? ceil_div(n, ranks) : 0;
+  p->nb_full = p->S > 0 ? ceil_div(p->S, block) : 0;
+  if (p->nb_full >= kMaxShardBlocks) {
+    delete p;
+    return CIERA_E_INVAL;
+  }
+  p->T = block >= kTileElems ? 1 : kTileElems / block;
+  p->tiles_full = ceil_div(p->nb_full, p->T);
+  p->r_full = p->S > 0 ? n / p->S : 0;
+  p->len_part = n - p->r_full * p->S;
+  p->tiles_part = p->len_part > 0 ? ceil_div(ceil_div(p->len_part, block), p->T) : 0;
+  p->total_tiles = p->r_full * p->tiles_full + p->tiles_part;
+  p->capacity = align_up(2 * p->S > 0 ? 2 * p->S : 1, 256);
+  p->flag_stride = align_up(p->nb_full > 0 ? p->nb_full : 1, 16);
+  p->nw_stride = ceil_div(p->nb_full > 0 ? p->nb_full : 1, 32);
+  p->off_status = 256;
+  p->off_flags = align_up(p->off_status + 8 * (p->total_tiles + 1), 256);
+  p->off_words = align_up(p->off_flags + p->flag_stride * ranks, 256);
+  p->off_prefix = align_up(p->off_words + 4 * p->nw_stride * ranks, 256);
+  p->off_rstate = align_up(p->off_prefix + 4 * p->nw_stride * ranks, 256);
+  p->ws_bytes = align_up(p->off_rstate + 4 * static_cast<int64_t>(ranks), 256);
+  p->fast = (block % 16 == 0) && block >= kFastMinBlock && block <= kFastMaxBlock &&
+            (p->S % 16 == 0);
+  p->smem_bytes = p->fast ? 4 * p->T * block : 0;
+  p->raw_fixup = raw_can_hold_unchanged(p->S, block) ||
+                 raw_can_hold_unchanged(p->len_part, block);
+  *out = p;
+  return CIERA_OK;
+}
+
+int ciera_plan_info(ciera_plan_t p, ciera_plan_info_t* info) {
+  if (!p || !info) return CIERA_E_INVAL;
+  info->numel = p->numel;
+  info->ranks = p->ranks;
+  info->block = p->block;
+  info->shard_len = p->S;
+  info->blocks_per_shard = p->nb_full;
+  info->tile_blocks = p->T;
+  info->total_tiles = p->total_tiles;
+  info->payload_capacity = p->capacity;
+  info->workspace_bytes = p->ws_bytes;
+  info->fast_path = p->fast ? 1 : 0;
+  info->raw_fixup = p->raw_fixup ? 1 : 0;
+  return CIERA_OK;
+}
+
+void ciera_plan_destroy(ciera_plan_t p) { delete p; }
+
+int ciera_workspace_init(ciera_plan_t p, void* workspace_dev, void* stream) {
+  if (!p || !workspace_dev) return CIERA_E_INVAL;
+  cudaError_t e = cudaMemsetAsync(workspace_dev, 0, static_cast<size_t>(p->ws_bytes),
+                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CIERA_OK : CIERA_E_CUDA;
+}
+
+int ciera_compress(ciera_plan_t p, int rank_begin, int rank_count, const uint16_t* w_dev,
+                   uint8_t* sender_cache_dev, uint8_t* payloads_dev, int64_t payload_stride,
+                   ciera_desc* descs_dev, uint8_t* flags_dev, void* workspace_dev, uint32_t flags,
+                   void* stream) {
+  if (!p || rank_begin < 0 || rank_count < 1 ||
+      static_cast<int64_t>(rank_begin) + rank_count > p->ranks)
+    return CIERA_E_INVAL;
+  if (!payloads_dev || !descs_dev || !workspace_dev || payload_stride < p->capacity)
+    return CIERA_E_INVAL;
+  const Geometry g = range_geometry(p, rank_begin, rank_count);
+  if (g.total_tiles > 0 && (!w_dev || !sender_cache_dev)) return CIERA_E_INVAL;
+  const uint32_t known = CIERA_COLD | CIERA_DEBUG_SKIP_FIRST_PUBLISH;
+  if (flags & ~known) return CIERA_E_INVAL;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace_dev);
+  CompressParams kp{};
+  kp.geo = g;
+  kp.w = w_dev;
+  kp.scache = sender_cache_dev;
+  kp.payloads = payloads_dev;
+  kp.stride = payload_stride;
+  kp.descs = descs_dev;
+  kp.flagbytes = flags_dev ? flags_dev : ws + p->off_flags;
+  kp.flag_stride = flags_dev ? p->nb_full : p->flag_stride;
+  kp.tile_status = reinterpret_cast<unsigned long long*>(ws + p->off_status);
+  kp.ctl = reinterpret_cast<Control*>(ws);
+  kp.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  kp.epoch = next_epoch();
+  kp.flags = flags;
+  kp.fast = p->fast && aligned16(w_dev) && aligned16(sender_cache_dev) &&
+            aligned16(payloads_dev) && (payload_stride % 16 == 0);
+  const int e = launch_compress(kp, kp.fast ? p->smem_bytes : 0, p->raw_fixup ? 1 : 0, stream);
+  return e == cudaSuccess ? CIERA_OK : CIERA_E_CUDA;
+}
+
+int ciera_decompress(ciera_plan_t p, const uint8_t* payloads_dev, int64_t payload_stride,
+                     const ciera_desc* descs_dev, uint8_t* recv_cache_dev, uint16_t* out_dev,
+                     void* workspace_dev, uint32_t flags, void* stream) {
+  if (!p || !payloads_dev || !descs_dev || !workspace_dev || payload_stride < p->capacity ||
+      flags != 0)
+    return CIERA_E_INVAL;
+  if (p->numel > 0 && (!recv_cache_dev || !out_dev)) return CIERA_E_INVAL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace_dev);
+  DecompressParams kp{};
+  kp.geo = range_geometry(p, 0, p->ranks);
+  kp.payloads = payloads_dev;
+  kp.stride = payload_stride;
+  kp.descs = descs_dev;
+  kp.rcache = recv_cache_dev;
+  kp.out = out_dev;
+  kp.bm_words = reinterpret_cast<uint32_t*>(ws + p->off_words);
+  kp.bm_prefix = reinterpret_cast<uint32_t*>(ws + p->off_prefix);
+  kp.nw_stride = p->nw_stride;
+  kp.rank_state = reinterpret_cast<uint32_t*>(ws + p->off_rstate);
+  kp.ctl = reinterpret_cast<Control*>(ws);
+  kp.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  kp.fast = p->fast && aligned16(payloads_dev) && (payload_stride % 16 == 0) &&
+            aligned16(recv_cache_dev) && aligned16(out_dev);
+  const int e = launch_decompress(kp, kp.fast ? p->smem_bytes : 0, stream);
+  return e == cudaSuccess ? CIERA_OK : CIERA_E_CUDA;
+}
+
+int ciera_status(void* workspace_dev, void* stream) {
+  if (!workspace_dev) return CIERA_E_INVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Control* ctl = static_cast<Control*>(workspace_dev);
+  uint32_t status = 0;
+  if (cudaMemcpyAsync(&status, &ctl->status, sizeof(status), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return CIERA_E_CUDA;
+  if (status != 0) {
+    if (cudaMemsetAsync(&ctl->status, 0, sizeof(uint32_t), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return CIERA_E_CUDA;
+  }
+  if (status & kStatusTimeout) return CIERA_E_TIMEOUT;
+  if (status & kStatusCorrupt) return CIERA_E_CORRUPT;
+  return CIERA_OK;
+}
+
+int ciera_should_compress(int64_t numel) {
+  ciera_cost_model m;
+  {
+    std::lock_guard<std::mutex> lk(g_cost_mu);
+    m = g_cost;
+  }
+  if (numel <= 0) return 0;
+  // Section 3.2: expected payload S_s+m + S_bm + q*S_e for a bf16 tensor
+  // (S_s+m = S_e = N bytes); the link time it saves must exceed the
+  // receiver's reconstruction time, the one kernel left on the critical path
+  // once compression overlaps compute.
+  const double n = static_cast<double>(numel);
+  const double bitmap = static_cast<double>(ceil_div(ceil_div(numel, m.block), 8));
+  const double payload = n + m.q_hat * n + bitmap;
+  const double saved_s = (2.0 * n - payload) / m.link_Bps;
+  const double decompress_s = m.t_fixed_s + (4.0 + m.q_hat) * n / m.hbm_Bps;
+  return saved_s > decompress_s ? 1 : 0;
+}
+
+int ciera_set_cost_model(const ciera_cost_model* model) {
+  if (!model || !(model->link_Bps > 0) || !(model->hbm_Bps > 0) || !(model->q_hat >= 0) ||
+      !(model->q_hat <= 1) || !(model->t_fixed_s >= 0) || model->block < 1)
+    return CIERA_E_INVAL;
+  std::lock_guard<std::mutex> lk(g_cost_mu);
+  g_cost = *model;
+  return CIERA_OK;
+}
+
+int ciera_get_cost_model(ciera_cost_model* model) {
+  if (!model) return CIERA_E_INVAL;
+  std::lock_guard<std::mutex> lk(g_cost_mu);
+  *model = g_cost;
+  return CIERA_OK;
+}
+
+int ciera_set_wait_timeout_ns(uint64_t ns) {
+  if (ns == 0) return CIERA_E_INVAL;
+  g_timeout_ns.store(ns, std::memory_order_relaxed);
+  return CIERA_OK;
+}
+
+}  // extern "C"

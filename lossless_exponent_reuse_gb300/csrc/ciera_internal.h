@@ -1,0 +1,92 @@
+// ciera_internal.h -- launch parameters shared by the host API and the kernels
+// of libciera.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#include "ciera.h"
+
+namespace ciera {
+
+constexpr int kThreads = 128;             // threads per CTA of the tile kernels
+constexpr int kScanThreads = 256;         // threads per CTA of the bitmap scan
+constexpr int64_t kTileElems = 4096;      // target values per tile (T*B)
+constexpr int kMaxTileBlocks = 4096;      // T <= 4096 (B = 1)
+constexpr int kMaxTileWords = kMaxTileBlocks / 32;
+constexpr int64_t kFastMinBlock = 256;    // fast path: T <= 16 blocks per tile
+constexpr int64_t kFastMaxBlock = 16384;  // fast path: <= 64 KB of staging per CTA
+constexpr int64_t kMaxNumel = int64_t(1) << 40;
+constexpr int64_t kMaxShardBlocks = int64_t(1) << 30;  // fits the 30-bit prefix field
+
+// Workspace control block at offset 0.
+struct Control {
+  uint32_t ticket;   // compress: next tile ticket; the last ticket resets it
+  uint32_t status;   // kStatus* bits, read and cleared by ciera_status
+  uint32_t pad[62];
+};
+enum : uint32_t { kStatusCorrupt = 1u, kStatusTimeout = 2u };
+
+// Decoupled look-back status word of one tile:
+//   bits 63..32 epoch of the call, bits 31..30 state, bits 29..0 count of
+//   changed blocks (aggregate of the tile, or inclusive prefix in its shard).
+enum : uint32_t { kStateAggregate = 1u, kStateInclusive = 2u };
+
+// Receiver per-rank state written by the bitmap scan.
+enum : uint32_t { kRankSkip = 0u, kRankCompressed = 1u, kRankRaw = 2u };
+
+// Shard/tile geometry of a contiguous rank range.  Inside any range the
+// full shards come first, then at most one partial shard, then empty ones.
+struct Geometry {
+  int64_t S;           // shard size ceil(N/R)
+  int64_t B;           // block size
+  int64_t T;           // blocks per tile
+  int64_t tiles_full;  // tiles of a full shard
+  int64_t len_part;    // values of the partial shard in range (0 if none)
+  int64_t tiles_part;  // its tiles
+  int64_t total_tiles;
+  int32_t nfull;       // full shards in range
+  int32_t has_part;    // partial shard present (range-local index nfull)
+  int32_t rank_count;  // ranks in range, empty ones included
+  int32_t pad;
+};
+
+struct CompressParams {
+  Geometry geo;
+  const uint16_t* w;            // first value of the range's first shard
+  uint8_t* scache;              // sender exponent cache, same origin
+  uint8_t* payloads;            // slot i at payloads + i*stride
+  int64_t stride;
+  ciera_desc* descs;
+  uint8_t* flagbytes;           // per-rank rows of flag_stride bytes
+  int64_t flag_stride;
+  unsigned long long* tile_status;
+  Control* ctl;
+  uint64_t timeout_ns;
+  uint32_t epoch;
+  uint32_t flags;
+  int32_t fast;                 // staged path allowed for whole-16 tiles
+  int32_t pad;
+};
+
+struct DecompressParams {
+  Geometry geo;                 // all R ranks
+  const uint8_t* payloads;
+  int64_t stride;
+  const ciera_desc* descs;
+  uint8_t* rcache;              // N exponent bytes
+  uint16_t* out;                // N values
+  uint32_t* bm_words;           // per rank: nw_stride aligned bitmap words
+  uint32_t* bm_prefix;          // per rank: exclusive popcount prefix per word
+  int64_t nw_stride;
+  uint32_t* rank_state;         // per rank: kRank*
+  Control* ctl;
+  uint64_t timeout_ns;
+  int32_t fast;
+  int32_t pad;
+};
+
+// Launchers (ciera_kernels.cu).  Return a cudaError_t value.
+int launch_compress(const CompressParams& p, int64_t smem_bytes, int raw_fixup, void* stream);
+int launch_decompress(const DecompressParams& p, int64_t smem_bytes, void* stream);
+
+}  // namespace ciera

@@ -1,0 +1,840 @@
+// ciera_kernels.cu -- sm_103a kernels of libciera.
+//
+// Method: "CIERA: Cross-Iteration Exponent Reuse for Lossless Allgather in
+// Sharded MoE Training", Section 3.1 (Exponent Reuse) and Appendix A,
+// Algorithm 1.  The paper's sender hashes each block's exponents and ANS-codes
+// changed exponents; here a block is compared exactly against the sender's
+// cached exponents and a changed block travels as its bf16 values, and the
+// receiver merges cached exponents with sign+mantissa bytes.
+//
+// Kernels (one CTA per tile of T consecutive blocks of one shard):
+//   k_compress       split + compare + per-block flags, decoupled look-back
+//                    over the count of changed blocks (the paper's "j <- j+1"
+//                    over the bitmap, as a single-pass scan), pack, sender
+//                    cache refresh, and -- in the shard's last tile -- the
+//                    descriptor and the bitmap.
+//   k_raw_fixup      only for plans where a raw payload can still contain
+//                    unchanged blocks (tiny B): rewrites such payloads raw.
+//   k_bitmap_scan    receiver: validates each descriptor against its bitmap
+//                    and writes per-word exclusive popcount prefixes.
+//   k_decompress     receiver: fused multi-rank gather + merge + ExpCache
+//                    refresh.
+// Tiles whose values are all whole 16-value groups use the staged path:
+// cp.async.bulk copies into shared memory, completion on an mbarrier, and
+// bulk stores back; other tiles use a byte-wise path with the same output.
+// Every wait (mbarrier, look-back) is bounded by a timeout that records
+// kStatusTimeout and lets the CTA finish.
+#include <cuda_runtime.h>
+
+#include "ciera_internal.h"
+
+namespace ciera {
+namespace {
+
+// ------------------------------------------------------------------------
+// PTX helpers
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Makes the mbarrier initialisation visible to the bulk-copy (async) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (bulk copy) reads of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for phase `parity` of an mbarrier.  False on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > timeout_ns) return false;
+  }
+  return true;
+}
+
+// Global -> shared bulk copy, completion counted on `bar` (bytes % 16 == 0,
+// both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Shared -> global bulk copy in the current bulk group.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_addr(src)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until every committed bulk store has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ------------------------------------------------------------------------
+// bf16 field arithmetic on packed words (two values per 32-bit word).
+// exponent e = (w >> 7) & 0xFF; sign+mantissa byte s = sign << 7 | mantissa.
+
+// Exponents of the 4 values in words a (values 0,1) and b (values 2,3).
+__device__ __forceinline__ uint32_t exp4(uint32_t a, uint32_t b) {
+  const uint32_t ea = ((a >> 7) & 0xFFu) | ((a >> 15) & 0xFF00u);
+  const uint32_t eb = ((b >> 7) & 0xFFu) | ((b >> 15) & 0xFF00u);
+  return ea | (eb << 16);
+}
+
+// Sign+mantissa bytes of the two values of word a.
+__device__ __forceinline__ uint32_t sm2(uint32_t a) {
+  return ((a >> 8) & 0x80u) | (a & 0x7Fu) | ((a >> 16) & 0x8000u) | ((a >> 8) & 0x7F00u);
+}
+
+__device__ __forceinline__ uint32_t sm4(uint32_t a, uint32_t b) { return sm2(a) | (sm2(b) << 16); }
+
+// Two values from two sign+mantissa bytes (s, low 16 bits) and two exponents
+// (e, low 16 bits).
+__device__ __forceinline__ uint32_t join2(uint32_t s, uint32_t e) {
+  return ((s & 0x80u) << 8) | ((e & 0xFFu) << 7) | (s & 0x7Fu) | ((s & 0x8000u) << 16) |
+         ((e & 0xFF00u) << 15) | ((s & 0x7F00u) << 8);
+}
+
+__device__ __forceinline__ uint32_t exp1(uint32_t v) { return (v >> 7) & 0xFFu; }
+__device__ __forceinline__ uint32_t sm1(uint32_t v) { return ((v >> 8) & 0x80u) | (v & 0x7Fu); }
+__device__ __forceinline__ uint32_t join1(uint32_t s, uint32_t e) {
+  return ((s & 0x80u) << 8) | ((e & 0xFFu) << 7) | (s & 0x7Fu);
+}
+
+// ------------------------------------------------------------------------
+// Tile geometry
+
+struct Tile {
+  int32_t rl;       // range-local rank
+  int64_t t;        // tile index inside the shard
+  int64_t len;      // values of the shard
+  int64_t nb;       // blocks of the shard
+  int64_t tiles;    // tiles of the shard
+  int64_t k0;       // first block of the tile
+  int32_t nblk;     // blocks in the tile
+  int64_t e0;       // first value of the tile, shard-relative
+  int64_t te;       // values in the tile
+  int64_t shard_off;  // first value of the shard, range-relative
+};
+
+__device__ __forceinline__ Tile decode_tile(const Geometry& g, int64_t i) {
+  Tile x;
+  const int64_t nf = static_cast<int64_t>(g.nfull) * g.tiles_full;
+  if (i < nf) {
+    x.rl = static_cast<int32_t>(i / g.tiles_full);
+    x.t = i - static_cast<int64_t>(x.rl) * g.tiles_full;
+    x.len = g.S;
+    x.tiles = g.tiles_full;
+  } else {
+    x.rl = g.nfull;
+    x.t = i - nf;
+    x.len = g.len_part;
+    x.tiles = g.tiles_part;
+  }
+  x.nb = (x.len + g.B - 1) / g.B;
+  x.k0 = x.t * g.T;
+  const int64_t nblk = x.nb - x.k0 < g.T ? x.nb - x.k0 : g.T;
+  x.nblk = static_cast<int32_t>(nblk);
+  x.e0 = x.k0 * g.B;
+  const int64_t te = x.len - x.e0;
+  x.te = te < nblk * g.B ? te : nblk * g.B;
+  x.shard_off = static_cast<int64_t>(x.rl) * g.S;
+  return x;
+}
+
+__device__ __forceinline__ int64_t shard_len_of(const Geometry& g, int32_t rl) {
+  if (rl < g.nfull) return g.S;
+  if (rl == g.nfull && g.has_part) return g.len_part;
+  return 0;
+}
+
+// Changed blocks before block kb of the tile (kb < nblk), from the tile's
+// flag words and their exclusive prefix.
+__device__ __forceinline__ uint32_t count_before(const uint32_t* fw, const uint32_t* fpre,
+                                                 int kb) {
+  const uint32_t mask = (kb & 31) ? (0xffffffffu >> (32 - (kb & 31))) : 0u;
+  return fpre[kb >> 5] + __popc(fw[kb >> 5] & mask);
+}
+
+__device__ __forceinline__ bool flag_of(const uint32_t* fw, int kb) {
+  return (fw[kb >> 5] >> (kb & 31)) & 1u;
+}
+
+// ------------------------------------------------------------------------
+// Decoupled look-back over the per-tile count of changed blocks (warp 0).
+// Publishes this tile's aggregate, sums predecessors' aggregates until an
+// inclusive prefix is found, publishes the inclusive prefix and returns the
+// exclusive one (clamped to k0 so that every offset stays in bounds even
+// after a timeout).
+
+__device__ uint32_t lookback(const CompressParams& p, int64_t g, const Tile& x, uint32_t agg,
+                             uint32_t lane, bool* timed_out) {
+  unsigned long long* st = p.tile_status;
+  const unsigned long long ep = static_cast<unsigned long long>(p.epoch) << 32;
+  const unsigned long long incl = static_cast<unsigned long long>(kStateInclusive) << 30;
+  const unsigned long long aggr = static_cast<unsigned long long>(kStateAggregate) << 30;
+  const bool skip_publish = (p.flags & CIERA_DEBUG_SKIP_FIRST_PUBLISH) && x.t == 0;
+  if (x.t == 0) {
+    if (lane == 0 && !skip_publish) st_release_u64(&st[g], ep | incl | agg);
+    return 0;
+  }
+  if (lane == 0) st_release_u64(&st[g], ep | aggr | agg);
+
+  const int64_t gfirst = g - x.t;
+  int64_t base = g - 1;
+  uint32_t X = 0;
+  bool to = false;
+  uint64_t t0 = 0;
+  bool started = false;
+  for (;;) {
+    const int64_t idx = base - static_cast<int64_t>(lane);
+    unsigned long long v = ep | incl;  // before the shard's first tile: inclusive 0
+    if (idx >= gfirst) {
+      for (;;) {
+        v = ld_acquire_u64(&st[idx]);
+        if ((v >> 32) == p.epoch && ((v >> 30) & 3ull) != 0) break;
+        const uint64_t now = globaltimer();
+        if (!started) {
+          t0 = now;
+          started = true;
+        } else if (now - t0 > p.timeout_ns) {
+          to = true;
+          v = ep | incl;
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+    if (__any_sync(0xffffffffu, to)) {
+      X = 0;
+      break;
+    }
+    const uint32_t is_incl = ((v >> 30) & 3ull) == kStateInclusive;
+    const uint32_t bal = __ballot_sync(0xffffffffu, is_incl);
+    const uint32_t val = static_cast<uint32_t>(v & 0x3FFFFFFFull);
+    if (bal) {
+      const int first = __ffs(bal) - 1;
+      X += warp_sum(static_cast<int>(lane) <= first ? val : 0u);
+      break;
+    }
+    X += warp_sum(val);
+    base -= 32;
+  }
+  if (X > static_cast<uint64_t>(x.k0)) X = static_cast<uint32_t>(x.k0);
+  if (lane == 0) st_release_u64(&st[g], ep | incl | (X + agg));
+  *timed_out = __any_sync(0xffffffffu, to);
+  return X;
+}
+
+// ------------------------------------------------------------------------
+// Compress: shared state of one CTA
+
+struct CompressShared {
+  uint32_t ticket_lo, ticket_hi;
+  uint32_t X;
+  uint32_t agg;
+  uint32_t bad;  // a bounded wait ran out
+  uint32_t fw[kMaxTileWords + 1];    // flag bits of the tile's blocks
+  uint32_t fpre[kMaxTileWords + 1];  // exclusive popcount prefix of fw
+};
+
+__device__ __forceinline__ void record_status(Control* ctl, uint32_t bits) {
+  atomicOr(&ctl->status, bits);
+}
+
+// Flag bytes, aggregate, look-back; leaves sh.X and sh.fpre ready.
+__device__ void compress_publish(const CompressParams& p, int64_t g, const Tile& x,
+                                 CompressShared& sh) {
+  const int tid = threadIdx.x;
+  const int nw = (x.nblk + 31) >> 5;
+  uint8_t* fb = p.flagbytes + static_cast<int64_t>(x.rl) * p.flag_stride + x.k0;
+  for (int kb = tid; kb < x.nblk; kb += blockDim.x) fb[kb] = flag_of(sh.fw, kb) ? 1 : 0;
+  if (tid == 0) {
+    uint32_t run = 0;
+    for (int i = 0; i < nw; ++i) {
+      sh.fpre[i] = run;
+      run += __popc(sh.fw[i]);
+    }
+    sh.agg = run;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid < 32) {
+    bool to = false;
+    const uint32_t X = lookback(p, g, x, sh.agg, tid, &to);
+    if (tid == 0) {
+      sh.X = X;
+      if (to) {
+        sh.bad = 1;
+        record_status(p.ctl, kStatusTimeout);
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
+// Last tile of a shard: descriptor and bitmap.
+__device__ void compress_epilogue(const CompressParams& p, const Tile& x,
+                                  const CompressShared& sh) {
+  const int tid = threadIdx.x;
+  const int64_t B = p.geo.B;
+  const uint32_t total = sh.X + sh.agg;  // changed blocks in the shard
+  const int64_t last_len = x.len - (x.nb - 1) * B;
+  const bool last_changed = flag_of(sh.fw, static_cast<int>(x.nb - 1 - x.k0));
+  const int64_t changed_vals =
+      static_cast<int64_t>(total) * B - (last_changed ? (B - last_len) : 0);
+  const int64_t body = x.len + changed_vals;
+  const int64_t bm = (x.nb + 7) / 8;
+  const bool raw = (p.flags & CIERA_COLD) || (body + bm >= 2 * x.len);
+  uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
+  if (tid == 0) {
+    ciera_desc d;
+    d.mode = raw ? CIERA_MODE_RAW : CIERA_MODE_COMPRESSED;
+    d.n_changed_blocks = total;
+    d.body_bytes = static_cast<uint64_t>(raw ? 2 * x.len : body);
+    d.payload_bytes = static_cast<uint64_t>(raw ? 2 * x.len : body + bm);
+    p.descs[x.rl] = d;
+  }
+  if (!raw) {
+    // every earlier tile wrote its flag bytes before publishing; the
+    // look-back's acquire chain makes them visible here
+    const uint8_t* fb = p.flagbytes + static_cast<int64_t>(x.rl) * p.flag_stride;
+    for (int64_t i = tid; i < bm; i += blockDim.x) {
+      uint32_t byte = 0;
+      for (int j = 0; j < 8; ++j) {
+        const int64_t k = 8 * i + j;
+        if (k < x.nb) byte |= static_cast<uint32_t>(fb[k] & 1u) << j;
+      }
+      payload[body + i] = static_cast<uint8_t>(byte);
+    }
+  }
+}
+
+// Byte-wise tile: any block size, any alignment.
+__device__ void compress_tile_bytes(const CompressParams& p, int64_t g, const Tile& x,
+                                    CompressShared& sh) {
+  const int tid = threadIdx.x;
+  const int64_t B = p.geo.B;
+  const uint16_t* w = p.w + x.shard_off + x.e0;
+  uint8_t* c = p.scache + x.shard_off + x.e0;
+  if (p.flags & CIERA_COLD) {
+    for (int kb = tid; kb < x.nblk; kb += blockDim.x) atomicOr(&sh.fw[kb >> 5], 1u << (kb & 31));
+  } else {
+    for (int64_t j = tid; j < x.te; j += blockDim.x) {
+      if (exp1(w[j]) != c[j]) {
+        const int kb = static_cast<int>(j / B);
+        atomicOr(&sh.fw[kb >> 5], 1u << (kb & 31));
+      }
+    }
+  }
+  __syncthreads();
+  compress_publish(p, g, x, sh);
+  uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
+  for (int64_t j = tid; j < x.te; j += blockDim.x) {
+    const int kb = static_cast<int>(j / B);
+    const int64_t within = j - kb * B;
+    const int64_t kg = x.k0 + kb;
+    const int64_t off = (kg + sh.X + count_before(sh.fw, sh.fpre, kb)) * B;
+    const uint32_t v = w[j];
+    if (flag_of(sh.fw, kb)) {
+      payload[off + 2 * within] = static_cast<uint8_t>(v & 0xFFu);
+      payload[off + 2 * within + 1] = static_cast<uint8_t>(v >> 8);
+      const uint8_t e = static_cast<uint8_t>(exp1(v));
+      if (c[j] != e) c[j] = e;
+    } else {
+      payload[off + within] = static_cast<uint8_t>(sm1(v));
+    }
+  }
+  __syncthreads();
+  if (x.t == x.tiles - 1) compress_epilogue(p, x, sh);
+}
+
+// Staged tile: T*B values, a multiple of 16, 16-byte aligned everywhere.
+// Shared memory: ws[2*TE] values | cs[TE] cached exponents | os[TE] sm bytes.
+__device__ void compress_tile_staged(const CompressParams& p, int64_t g, const Tile& x,
+                                     CompressShared& sh, uint8_t* dsm, uint64_t* bar) {
+  const int tid = threadIdx.x;
+  const int64_t B = p.geo.B;
+  const int64_t TE = p.geo.T * B;
+  uint8_t* ws = dsm;
+  uint8_t* cs = dsm + 2 * TE;
+  uint8_t* os = dsm + 3 * TE;
+  const uint16_t* w = p.w + x.shard_off + x.e0;
+  uint8_t* c = p.scache + x.shard_off + x.e0;
+  const uint32_t te = static_cast<uint32_t>(x.te);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(bar, 3u * te);
+    bulk_g2s(ws, w, 2u * te, bar);
+    bulk_g2s(cs, c, te, bar);
+  }
+  __syncthreads();
+  const bool ok = mbar_wait_bounded(bar, 0, p.timeout_ns);
+  if (__syncthreads_or(!ok)) {
+    // the copies did not land in time: record it, wait once more for them
+    // so that no copy is left writing into this CTA's shared memory
+    if (tid == 0) {
+      record_status(p.ctl, kStatusTimeout);
+      sh.bad = 1;
+    }
+    mbar_wait_bounded(bar, 0, p.timeout_ns);
+    __syncthreads();
+  }
+  const int ngroups = static_cast<int>(te >> 4);
+  const bool cold = p.flags & CIERA_COLD;
+  if (cold || sh.bad) {
+    for (int kb = tid; kb < x.nblk; kb += blockDim.x) atomicOr(&sh.fw[kb >> 5], 1u << (kb & 31));
+  } else {
+    for (int gi = tid; gi < ngroups; gi += blockDim.x) {
+      const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
+      const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
+      const uint4 cc = reinterpret_cast<const uint4*>(cs)[gi];
+      const uint32_t d = (exp4(w0.x, w0.y) ^ cc.x) | (exp4(w0.z, w0.w) ^ cc.y) |
+                         (exp4(w1.x, w1.y) ^ cc.z) | (exp4(w1.z, w1.w) ^ cc.w);
+      if (d) {
+        const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
+        atomicOr(&sh.fw[kb >> 5], 1u << (kb & 31));
+      }
+    }
+  }
+  __syncthreads();
+  compress_publish(p, g, x, sh);
+
+  // pack: sign+mantissa bytes of unchanged blocks into os; exponents of
+  // changed blocks into the sender cache (only the 16-byte groups that differ)
+  for (int gi = tid; gi < ngroups; gi += blockDim.x) {
+    const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
+    const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
+    const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
+    if (flag_of(sh.fw, kb)) {
+      const uint4 e = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w), exp4(w1.x, w1.y),
+                                 exp4(w1.z, w1.w));
+      const uint4 cc = reinterpret_cast<const uint4*>(cs)[gi];
+      if (cold || ((e.x ^ cc.x) | (e.y ^ cc.y) | (e.z ^ cc.z) | (e.w ^ cc.w)))
+        reinterpret_cast<uint4*>(c)[gi] = e;
+    } else {
+      reinterpret_cast<uint4*>(os)[gi] =
+          make_uint4(sm4(w0.x, w0.y), sm4(w0.z, w0.w), sm4(w1.x, w1.y), sm4(w1.z, w1.w));
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
+    int ka = 0;
+    while (ka < x.nblk) {
+      const bool f = flag_of(sh.fw, ka);
+      int kz = ka + 1;
+      while (kz < x.nblk && flag_of(sh.fw, kz) == f) ++kz;
+      const int64_t ea = static_cast<int64_t>(ka) * B;
+      const int64_t ez = static_cast<int64_t>(kz) * B < x.te ? static_cast<int64_t>(kz) * B : x.te;
+      const int64_t off = (x.k0 + ka + sh.X + count_before(sh.fw, sh.fpre, ka)) * B;
+      if (f)
+        bulk_s2g(payload + off, ws + 2 * ea, static_cast<uint32_t>(2 * (ez - ea)));
+      else
+        bulk_s2g(payload + off, os + ea, static_cast<uint32_t>(ez - ea));
+      ka = kz;
+    }
+    bulk_commit();
+  }
+  if (x.t == x.tiles - 1) compress_epilogue(p, x, sh);
+  if (tid == 0) bulk_wait_read_all();
+}
+
+__global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ CompressShared sh;
+  __shared__ __align__(8) uint64_t bar;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    // ticket order = start order: a tile only ever waits on tiles whose
+    // CTAs started earlier, so the look-back cannot wait on an unscheduled CTA
+    const uint32_t t = atomicAdd(&p.ctl->ticket, 1u);
+    if (t == gridDim.x - 1) atomicExch(&p.ctl->ticket, 0u);
+    sh.ticket_lo = t;
+    sh.bad = 0;
+  }
+  for (int i = tid; i <= kMaxTileWords; i += blockDim.x) sh.fw[i] = 0;
+  __syncthreads();
+  const int64_t g = sh.ticket_lo;
+  if (g >= p.geo.total_tiles) {
+    // the last ticket: descriptors of empty shards in the range
+    for (int32_t rl = p.geo.nfull + p.geo.has_part + tid; rl < p.geo.rank_count;
+         rl += blockDim.x) {
+      ciera_desc d;
+      d.mode = CIERA_MODE_RAW;
+      d.n_changed_blocks = 0;
+      d.body_bytes = 0;
+      d.payload_bytes = 0;
+      p.descs[rl] = d;
+    }
+    return;
+  }
+  const Tile x = decode_tile(p.geo, g);
+  if (p.fast && (x.te & 15) == 0)
+    compress_tile_staged(p, g, x, sh, dsm, &bar);
+  else
+    compress_tile_bytes(p, g, x, sh);
+}
+
+// A raw payload whose body was written in compressed layout (possible only
+// when an unchanged block is not larger than the bitmap): copy the shard.
+__global__ void __launch_bounds__(kThreads) k_raw_fixup(const CompressParams p) {
+  const Tile x = decode_tile(p.geo, blockIdx.x);
+  const ciera_desc d = p.descs[x.rl];
+  if (d.mode != CIERA_MODE_RAW || d.n_changed_blocks >= x.nb) return;
+  const uint16_t* w = p.w + x.shard_off + x.e0;
+  uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride + 2 * x.e0;
+  for (int64_t j = threadIdx.x; j < x.te; j += blockDim.x) {
+    const uint32_t v = w[j];
+    payload[2 * j] = static_cast<uint8_t>(v & 0xFFu);
+    payload[2 * j + 1] = static_cast<uint8_t>(v >> 8);
+  }
+}
+
+// ------------------------------------------------------------------------
+// Receiver
+
+// One CTA per rank: validate the descriptor, copy the bitmap into aligned
+// words and write each word's exclusive popcount prefix.
+__global__ void __launch_bounds__(kScanThreads) k_bitmap_scan(const DecompressParams p) {
+  __shared__ uint32_t warp_tot[kScanThreads / 32];
+  __shared__ uint32_t s_total;
+  const int32_t r = blockIdx.x;
+  const int tid = threadIdx.x;
+  const Geometry& geo = p.geo;
+  const int64_t len = shard_len_of(geo, r);
+  const int64_t nb = (len + geo.B - 1) / geo.B;
+  const int64_t bm = (nb + 7) / 8;
+  const int64_t nw = (nb + 31) / 32;
+  const ciera_desc d = p.descs[r];
+  const uint8_t* payload = p.payloads + static_cast<int64_t>(r) * p.stride;
+
+  // the same decision in every thread of the CTA
+  uint32_t state = kRankSkip;
+  if (d.mode == CIERA_MODE_RAW) {
+    if (d.body_bytes == static_cast<uint64_t>(2 * len) && d.payload_bytes == d.body_bytes &&
+        d.n_changed_blocks <= nb)
+      state = kRankRaw;
+  } else if (d.mode == CIERA_MODE_COMPRESSED && len > 0) {
+    if (d.body_bytes >= static_cast<uint64_t>(len) &&
+        d.payload_bytes == d.body_bytes + static_cast<uint64_t>(bm) &&
+        d.payload_bytes < static_cast<uint64_t>(2 * len) &&
+        d.payload_bytes <= static_cast<uint64_t>(p.stride))
+      state = kRankCompressed;
+  }
+  if (state == kRankCompressed) {
+    const uint8_t* bitmap = payload + d.body_bytes;
+    uint32_t* words = p.bm_words + static_cast<int64_t>(r) * p.nw_stride;
+    uint32_t* pre = p.bm_prefix + static_cast<int64_t>(r) * p.nw_stride;
+    const int64_t per = (nw + kScanThreads - 1) / kScanThreads;
+    const int64_t lo = tid * per < nw ? tid * per : nw;
+    const int64_t hi = lo + per < nw ? lo + per : nw;
+    uint32_t local = 0;
+    uint32_t pad_bad = 0;
+    for (int64_t i = lo; i < hi; ++i) {
+      uint32_t word = 0;
+      for (int j = 0; j < 4; ++j) {
+        const int64_t b = 4 * i + j;
+        if (b < bm) word |= static_cast<uint32_t>(bitmap[b]) << (8 * j);
+      }
+      if (i == nw - 1 && (nb & 31)) {
+        // bits past the last block must be zero
+        pad_bad = (word >> (nb & 31)) != 0;
+        word &= 0xffffffffu >> (32 - (nb & 31));
+      }
+      words[i] = word;
+      local += __popc(word);
+    }
+    // block-wide exclusive scan of the per-thread popcounts
+    const int lane = tid & 31, wid = tid >> 5;
+    uint32_t incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    uint32_t wbase = 0;
+    for (int i = 0; i < wid; ++i) wbase += warp_tot[i];
+    if (tid == kScanThreads - 1) s_total = wbase + incl;
+    uint32_t run = wbase + incl - local;
+    for (int64_t i = lo; i < hi; ++i) {
+      pre[i] = run;
+      run += __popc(words[i]);
+    }
+    const uint32_t any_pad_bad = __syncthreads_or(pad_bad);
+    if (tid == 0) {
+      const uint32_t total = s_total;
+      const int64_t last_len = len - (nb - 1) * geo.B;
+      const bool last_changed = (words[nw - 1] >> ((nb - 1) & 31)) & 1u;
+      const int64_t changed_vals =
+          static_cast<int64_t>(total) * geo.B - (last_changed ? geo.B - last_len : 0);
+      const bool consistent = !any_pad_bad && total == d.n_changed_blocks &&
+                              d.body_bytes == static_cast<uint64_t>(len + changed_vals);
+      if (!consistent) state = kRankSkip;
+    }
+  }
+  if (tid == 0) {
+    if (state == kRankSkip) atomicOr(&p.ctl->status, kStatusCorrupt);
+    p.rank_state[r] = state;
+  }
+}
+
+struct DecompressShared {
+  uint32_t X;
+  uint32_t bad;
+  uint32_t fw[2];  // flag bits of the tile's blocks (staged path: T <= 16)
+};
+
+// Byte-wise tile of the receiver.
+__device__ void decompress_tile_bytes(const DecompressParams& p, const Tile& x, uint32_t state) {
+  const int64_t B = p.geo.B;
+  const uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
+  uint8_t* rc = p.rcache + x.shard_off + x.e0;
+  uint16_t* out = p.out + x.shard_off + x.e0;
+  if (state == kRankRaw) {
+    for (int64_t j = threadIdx.x; j < x.te; j += blockDim.x) {
+      const int64_t o = 2 * (x.e0 + j);
+      const uint32_t v = payload[o] | (static_cast<uint32_t>(payload[o + 1]) << 8);
+      out[j] = static_cast<uint16_t>(v);
+      rc[j] = static_cast<uint8_t>(exp1(v));
+    }
+    return;
+  }
+  const uint32_t* words = p.bm_words + static_cast<int64_t>(x.rl) * p.nw_stride;
+  const uint32_t* pre = p.bm_prefix + static_cast<int64_t>(x.rl) * p.nw_stride;
+  for (int64_t j = threadIdx.x; j < x.te; j += blockDim.x) {
+    const int64_t kg = x.k0 + j / B;
+    const int64_t within = x.e0 + j - kg * B;
+    const uint32_t word = words[kg >> 5];
+    const uint32_t bit = static_cast<uint32_t>(kg & 31);
+    const uint32_t C = pre[kg >> 5] + __popc(word & (bit ? (0xffffffffu >> (32 - bit)) : 0u));
+    const int64_t off = (kg + C) * B;
+    if ((word >> bit) & 1u) {
+      const int64_t o = off + 2 * within;
+      const uint32_t v = payload[o] | (static_cast<uint32_t>(payload[o + 1]) << 8);
+      out[j] = static_cast<uint16_t>(v);
+      rc[j] = static_cast<uint8_t>(exp1(v));
+    } else {
+      out[j] = static_cast<uint16_t>(join1(payload[off + within], rc[j]));
+    }
+  }
+}
+
+// Staged tile of the receiver.  Shared memory: ws[2*TE] | ss[TE] | cs[TE].
+__device__ void decompress_tile_staged(const DecompressParams& p, const Tile& x, uint32_t state,
+                                       DecompressShared& sh, uint8_t* dsm, uint64_t* bar) {
+  const int tid = threadIdx.x;
+  const int64_t B = p.geo.B;
+  const int64_t TE = p.geo.T * B;
+  uint8_t* ws = dsm;
+  uint8_t* ss = dsm + 2 * TE;
+  uint8_t* cs = dsm + 3 * TE;
+  const uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
+  uint8_t* rc = p.rcache + x.shard_off + x.e0;
+  uint16_t* out = p.out + x.shard_off + x.e0;
+  const uint32_t te = static_cast<uint32_t>(x.te);
+  const bool raw = state == kRankRaw;
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+    if (raw) {
+      sh.fw[0] = 0xffffffffu;
+      sh.X = 0;
+      mbar_arrive_expect_tx(bar, 2u * te);
+      bulk_g2s(ws, payload + 2 * x.e0, 2u * te, bar);
+    } else {
+      // flag bits of blocks k0 .. k0+nblk-1 (nblk <= 16, may straddle a word)
+      const uint32_t* words = p.bm_words + static_cast<int64_t>(x.rl) * p.nw_stride;
+      const uint32_t* pre = p.bm_prefix + static_cast<int64_t>(x.rl) * p.nw_stride;
+      const int64_t wi = x.k0 >> 5;
+      const uint32_t sh0 = static_cast<uint32_t>(x.k0 & 31);
+      const uint64_t two = static_cast<uint64_t>(words[wi]) |
+                           ((wi + 1 < (x.nb + 31) / 32) ? static_cast<uint64_t>(words[wi + 1]) << 32
+                                                        : 0ull);
+      const uint32_t fw = static_cast<uint32_t>(two >> sh0) &
+                          (x.nblk >= 32 ? 0xffffffffu : ((1u << x.nblk) - 1u));
+      const uint32_t X =
+          pre[wi] + __popc(words[wi] & (sh0 ? (0xffffffffu >> (32 - sh0)) : 0u));
+      sh.fw[0] = fw;
+      sh.X = X;
+      // a changed value brings 2 payload bytes, a kept one 1 payload byte
+      // and 1 cached exponent: 2 bytes of shared memory per value either way
+      uint32_t before = 0;
+      int ka = 0;
+      mbar_arrive_expect_tx(bar, 2u * te);
+      while (ka < x.nblk) {
+        const bool f = (fw >> ka) & 1u;
+        int kz = ka + 1;
+        while (kz < x.nblk && (((fw >> kz) & 1u) != 0) == f) ++kz;
+        const int64_t ea = static_cast<int64_t>(ka) * B;
+        const int64_t ez = static_cast<int64_t>(kz) * B < x.te ? static_cast<int64_t>(kz) * B : x.te;
+        const int64_t off = (x.k0 + ka + X + before) * B;
+        if (f) {
+          bulk_g2s(ws + 2 * ea, payload + off, static_cast<uint32_t>(2 * (ez - ea)), bar);
+          before += static_cast<uint32_t>(kz - ka);
+        } else {
+          bulk_g2s(ss + ea, payload + off, static_cast<uint32_t>(ez - ea), bar);
+          bulk_g2s(cs + ea, rc + ea, static_cast<uint32_t>(ez - ea), bar);
+        }
+        ka = kz;
+      }
+    }
+  }
+  __syncthreads();
+  const bool ok = mbar_wait_bounded(bar, 0, p.timeout_ns);
+  if (__syncthreads_or(!ok)) {
+    if (tid == 0) record_status(p.ctl, kStatusTimeout);
+    mbar_wait_bounded(bar, 0, p.timeout_ns);
+    __syncthreads();
+    return;
+  }
+  const uint32_t fw = sh.fw[0];
+  const int ngroups = static_cast<int>(te >> 4);
+  for (int gi = tid; gi < ngroups; gi += blockDim.x) {
+    const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
+    if (raw || ((fw >> kb) & 1u)) {
+      const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
+      const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
+      reinterpret_cast<uint4*>(rc)[gi] = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w),
+                                                    exp4(w1.x, w1.y), exp4(w1.z, w1.w));
+    } else {
+      const uint4 s = reinterpret_cast<const uint4*>(ss)[gi];
+      const uint4 e = reinterpret_cast<const uint4*>(cs)[gi];
+      reinterpret_cast<uint4*>(ws)[2 * gi] =
+          make_uint4(join2(s.x, e.x), join2(s.x >> 16, e.x >> 16), join2(s.y, e.y),
+                     join2(s.y >> 16, e.y >> 16));
+      reinterpret_cast<uint4*>(ws)[2 * gi + 1] =
+          make_uint4(join2(s.z, e.z), join2(s.z >> 16, e.z >> 16), join2(s.w, e.w),
+                     join2(s.w >> 16, e.w >> 16));
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    bulk_s2g(out, ws, 2u * te);
+    bulk_commit();
+    bulk_wait_read_all();
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_decompress(const DecompressParams p) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ DecompressShared sh;
+  __shared__ __align__(8) uint64_t bar;
+  const Tile x = decode_tile(p.geo, blockIdx.x);
+  const uint32_t state = p.rank_state[x.rl];
+  if (state == kRankSkip) return;
+  if (p.fast && (x.te & 15) == 0)
+    decompress_tile_staged(p, x, state, sh, dsm, &bar);
+  else
+    decompress_tile_bytes(p, x, state);
+}
+
+}  // namespace
+
+int launch_compress(const CompressParams& p, int64_t smem_bytes, int raw_fixup, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (smem_bytes > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_compress, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_bytes));
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t grid = p.geo.total_tiles + 1;
+  k_compress<<<static_cast<unsigned>(grid), kThreads, static_cast<size_t>(smem_bytes), s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (raw_fixup && p.geo.total_tiles > 0) {
+    k_raw_fixup<<<static_cast<unsigned>(p.geo.total_tiles), kThreads, 0, s>>>(p);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+int launch_decompress(const DecompressParams& p, int64_t smem_bytes, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (smem_bytes > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(
+        k_decompress, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
+    if (e != cudaSuccess) return e;
+  }
+  if (p.geo.rank_count > 0) {
+    k_bitmap_scan<<<static_cast<unsigned>(p.geo.rank_count), kScanThreads, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (p.geo.total_tiles > 0) {
+    k_decompress<<<static_cast<unsigned>(p.geo.total_tiles), kThreads,
+                   static_cast<size_t>(smem_bytes), s>>>(p);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
+}
+
+}  // namespace ciera

@@ -1,0 +1,90 @@
+"""Parity harness: runs the same seeded weight sequence through libciera on
+the GPU and through the CPU oracle, and compares every output byte for byte:
+per-block flags, descriptors, payload bytes, the rebuilt tensor and both
+exponent caches."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from lossless_exponent_reuse_gb300 import ciera
+from lossless_exponent_reuse_gb300.allgather import SimulatedAllgather
+
+
+def exps_dev(w_u16: torch.Tensor) -> torch.Tensor:
+    """Exponent bytes of bf16 bit patterns, computed with torch ops (test side)."""
+    return ((w_u16.view(torch.int16).to(torch.int32) >> 7) & 0xFF).to(torch.uint8)
+
+
+def eq16(a: torch.Tensor, b: torch.Tensor) -> bool:
+    """Bitwise equality of two 16-bit tensors (compared as int16)."""
+    return torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def to_np_u16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def to_np_u8(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy()
+
+
+class OracleState:
+    def __init__(self, n, ranks, block):
+        self.n, self.ranks, self.block = n, ranks, block
+        self.scache = np.zeros(n, np.uint8)
+        self.rcache = np.zeros(n, np.uint8)
+        self.t = 0
+
+    def step(self, w: np.ndarray):
+        payloads, descs, flags = oracle.compress_plan(w, self.ranks, self.block, self.scache,
+                                                      cold=self.t == 0)
+        st, out = oracle.decompress_plan(payloads, descs, self.n, self.ranks, self.block,
+                                         self.rcache)
+        assert st == 0
+        self.t += 1
+        return payloads, descs, flags, out
+
+
+def compare_step(ag: SimulatedAllgather, ost: OracleState, w_np: np.ndarray, o_payloads,
+                 o_descs, o_flags, o_out, tag=""):
+    n, R, B = ost.n, ost.ranks, ost.block
+    g_descs = ag.descriptors()
+    g_payloads = to_np_u8(ag.payloads)
+    g_flags = to_np_u8(ag.flags)
+    for r in range(R):
+        od = o_descs[r]
+        gd = g_descs[r]
+        assert (gd["mode"], gd["n_changed_blocks"], gd["body_bytes"], gd["payload_bytes"]) == (
+            int(od["mode"]), int(od["n_changed_blocks"]), int(od["body_bytes"]),
+            int(od["payload_bytes"])), f"{tag} rank {r} descriptor"
+        pb = int(od["payload_bytes"])
+        if not np.array_equal(g_payloads[r, :pb], o_payloads[r, :pb]):
+            bad = np.nonzero(g_payloads[r, :pb] != o_payloads[r, :pb])[0]
+            raise AssertionError(f"{tag} rank {r} payload differs at {bad[:10]} of {pb}")
+        ln = oracle.shard_len(n, R, r)
+        nb = oracle.num_blocks(ln, B) if ln else 0
+        np.testing.assert_array_equal(g_flags[r, :nb], o_flags[r, :nb],
+                                      err_msg=f"{tag} rank {r} flags")
+    np.testing.assert_array_equal(to_np_u16(ag.out[:n]), o_out, err_msg=f"{tag} out")
+    np.testing.assert_array_equal(to_np_u8(ag.sender_cache[:n]), ost.scache,
+                                  err_msg=f"{tag} sender cache")
+    np.testing.assert_array_equal(to_np_u8(ag.recv_cache[:n]), ost.rcache,
+                                  err_msg=f"{tag} receiver cache")
+    np.testing.assert_array_equal(o_out, w_np, err_msg=f"{tag} oracle round trip")
+
+
+def run_parity(seq_np, ranks, block, device="cuda", tag=""):
+    """seq_np: list of uint16 numpy arrays (w_0, w_1, ...)."""
+    n = seq_np[0].size
+    ag = SimulatedAllgather(n, block, ranks, device=device, keep_flags=True)
+    ost = OracleState(n, ranks, block)
+    for t, w in enumerate(seq_np):
+        w_dev = torch.from_numpy(w.view(np.int16)).to(device).view(torch.uint16)
+        ag.step(w_dev)
+        st = ag.status()
+        assert st == ciera.OK, f"{tag} t={t} status {ciera.strerror(st)}"
+        o_payloads, o_descs, o_flags, o_out = ost.step(w)
+        compare_step(ag, ost, w, o_payloads, o_descs, o_flags, o_out, tag=f"{tag} t={t}")
+    return ag, ost
