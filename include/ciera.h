@@ -66,6 +66,7 @@ extern "C" {
 #define CIERA_E_CUDA (-2)        /* a CUDA runtime call failed */
 #define CIERA_E_CORRUPT (-3)     /* a received descriptor/bitmap does not match the plan */
 #define CIERA_E_TIMEOUT (-4)     /* a bounded device-side wait ran out */
+#define CIERA_E_INTERNAL (-5)    /* a kernel found its launch configuration inconsistent */
 
 #define CIERA_MODE_COMPRESSED 0u
 #define CIERA_MODE_RAW 1u
@@ -163,7 +164,8 @@ int ciera_decompress(ciera_plan_t plan, const uint8_t *payloads_dev, int64_t pay
                      void *workspace_dev, uint32_t flags, void *stream);
 
 /* Wait for `stream`, then read and clear the workspace's status word.
- * Returns CIERA_OK, CIERA_E_CORRUPT, CIERA_E_TIMEOUT or CIERA_E_CUDA. */
+ * Returns CIERA_OK, CIERA_E_CORRUPT, CIERA_E_TIMEOUT, CIERA_E_INTERNAL or
+ * CIERA_E_CUDA. */
 int ciera_status(void *workspace_dev, void *stream);
 
 /* Per-tensor predicate (Section 3.2): 1 = compress, 0 = send raw.

@@ -26,6 +26,7 @@ E_INVAL = -1
 E_CUDA = -2
 E_CORRUPT = -3
 E_TIMEOUT = -4
+E_INTERNAL = -5
 
 MODE_COMPRESSED = 0
 MODE_RAW = 1
@@ -232,7 +233,8 @@ class Plan:
 
 
 def status(workspace: torch.Tensor, stream=None) -> int:
-    """ciera_status: waits for the stream; returns OK, E_CORRUPT or E_TIMEOUT."""
+    """ciera_status: waits for the stream; returns OK, E_CORRUPT, E_TIMEOUT or
+    E_INTERNAL."""
     st = lib().ciera_status(_dev_ptr(workspace, "workspace", torch.uint8), _stream_handle(stream))
     if st == E_CUDA:
         raise CieraError(st, "ciera_status")

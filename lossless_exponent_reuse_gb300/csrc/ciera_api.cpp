@@ -33,7 +33,9 @@ struct ciera_plan_s {
   int64_t flag_stride;
   int64_t nw_stride;
   int64_t off_status, off_flags, off_words, off_prefix, off_rstate, ws_bytes;
-  int64_t smem_bytes;  // dynamic shared memory of the staged path
+  int64_t smem_flags;       // dynamic shared memory of every compress call
+  int64_t smem_compress;    // ... of a staged compress call
+  int64_t smem_decompress;
   bool fast;
   bool raw_fixup;
 };
@@ -99,6 +101,7 @@ const char* ciera_strerror(int status) {
     case CIERA_E_CUDA: return "CUDA runtime error";
     case CIERA_E_CORRUPT: return "corrupt descriptor or bitmap";
     case CIERA_E_TIMEOUT: return "bounded device wait timed out";
+    case CIERA_E_INTERNAL: return "internal launch configuration error";
     default: return "unknown status";
   }
 }
@@ -140,7 +143,11 @@ int ciera_plan(const int64_t* shape, int ndim, int64_t block, int ranks, ciera_p
   p->ws_bytes = align_up(p->off_rstate + 4 * static_cast<int64_t>(ranks), 256);
   p->fast = (block % 16 == 0) && block >= kFastMinBlock && block <= kFastMaxBlock &&
             (p->S % 16 == 0);
-  p->smem_bytes = p->fast ? 4 * p->T * block : 0;
+  // compress: flag words + their prefix (every call), then 2*TE values and
+  // TE exponents (staged calls only)
+  p->smem_flags = align_up(8 * ceil_div(p->T, 32), 128);
+  p->smem_compress = p->smem_flags + (p->fast ? 3 * p->T * block : 0);
+  p->smem_decompress = p->fast ? 4 * p->T * block : 0;
   p->raw_fixup = raw_can_hold_unchanged(p->S, block) ||
                  raw_can_hold_unchanged(p->len_part, block);
   *out = p;
@@ -203,7 +210,8 @@ int ciera_compress(ciera_plan_t p, int rank_begin, int rank_count, const uint16_
   kp.flags = flags;
   kp.fast = p->fast && aligned16(w_dev) && aligned16(sender_cache_dev) &&
             aligned16(payloads_dev) && (payload_stride % 16 == 0);
-  const int e = launch_compress(kp, kp.fast ? p->smem_bytes : 0, p->raw_fixup ? 1 : 0, stream);
+  const int e = launch_compress(kp, kp.fast ? p->smem_compress : p->smem_flags,
+                               p->raw_fixup ? 1 : 0, stream);
   return e == cudaSuccess ? CIERA_OK : CIERA_E_CUDA;
 }
 
@@ -230,7 +238,7 @@ int ciera_decompress(ciera_plan_t p, const uint8_t* payloads_dev, int64_t payloa
   kp.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   kp.fast = p->fast && aligned16(payloads_dev) && (payload_stride % 16 == 0) &&
             aligned16(recv_cache_dev) && aligned16(out_dev);
-  const int e = launch_decompress(kp, kp.fast ? p->smem_bytes : 0, stream);
+  const int e = launch_decompress(kp, kp.fast ? p->smem_decompress : 0, stream);
   return e == cudaSuccess ? CIERA_OK : CIERA_E_CUDA;
 }
 
@@ -248,6 +256,7 @@ int ciera_status(void* workspace_dev, void* stream) {
         cudaStreamSynchronize(s) != cudaSuccess)
       return CIERA_E_CUDA;
   }
+  if (status & kStatusInternal) return CIERA_E_INTERNAL;
   if (status & kStatusTimeout) return CIERA_E_TIMEOUT;
   if (status & kStatusCorrupt) return CIERA_E_CORRUPT;
   return CIERA_OK;

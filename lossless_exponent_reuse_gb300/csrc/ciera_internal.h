@@ -10,10 +10,10 @@ namespace ciera {
 
 constexpr int kThreads = 128;             // threads per CTA of the tile kernels
 constexpr int kScanThreads = 256;         // threads per CTA of the bitmap scan
-constexpr int64_t kTileElems = 4096;      // target values per tile (T*B)
-constexpr int kMaxTileBlocks = 4096;      // T <= 4096 (B = 1)
+constexpr int64_t kTileElems = 8192;      // target values per tile (T*B)
+constexpr int kMaxTileBlocks = 8192;      // T <= 8192 (B = 1)
 constexpr int kMaxTileWords = kMaxTileBlocks / 32;
-constexpr int64_t kFastMinBlock = 256;    // fast path: T <= 16 blocks per tile
+constexpr int64_t kFastMinBlock = 256;    // fast path: T <= 32 blocks per tile
 constexpr int64_t kFastMaxBlock = 16384;  // fast path: <= 64 KB of staging per CTA
 constexpr int64_t kMaxNumel = int64_t(1) << 40;
 constexpr int64_t kMaxShardBlocks = int64_t(1) << 30;  // fits the 30-bit prefix field
@@ -24,7 +24,7 @@ struct Control {
   uint32_t status;   // kStatus* bits, read and cleared by ciera_status
   uint32_t pad[62];
 };
-enum : uint32_t { kStatusCorrupt = 1u, kStatusTimeout = 2u };
+enum : uint32_t { kStatusCorrupt = 1u, kStatusTimeout = 2u, kStatusInternal = 4u };
 
 // Decoupled look-back status word of one tile:
 //   bits 63..32 epoch of the call, bits 31..30 state, bits 29..0 count of
@@ -86,6 +86,7 @@ struct DecompressParams {
 };
 
 // Launchers (ciera_kernels.cu).  Return a cudaError_t value.
+// smem_bytes: dynamic shared memory of one CTA.
 int launch_compress(const CompressParams& p, int64_t smem_bytes, int raw_fixup, void* stream);
 int launch_decompress(const DecompressParams& p, int64_t smem_bytes, void* stream);
 

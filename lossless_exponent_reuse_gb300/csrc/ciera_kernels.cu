@@ -26,6 +26,8 @@
 // kStatusTimeout and lets the CTA finish.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "ciera_internal.h"
 
 namespace ciera {
@@ -126,6 +128,13 @@ __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Bytes of dynamic shared memory this CTA was launched with.
+__device__ __forceinline__ uint32_t dynamic_smem_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -169,6 +178,7 @@ __device__ __forceinline__ uint32_t join1(uint32_t s, uint32_t e) {
 struct Tile {
   int32_t rl;       // range-local rank
   int64_t t;        // tile index inside the shard
+  int64_t sidx;     // shard-major tile index: rl * tiles_full + t
   int64_t len;      // values of the shard
   int64_t nb;       // blocks of the shard
   int64_t tiles;    // tiles of the shard
@@ -179,20 +189,14 @@ struct Tile {
   int64_t shard_off;  // first value of the shard, range-relative
 };
 
-__device__ __forceinline__ Tile decode_tile(const Geometry& g, int64_t i) {
+__device__ __forceinline__ Tile make_tile(const Geometry& g, int32_t rl, int64_t t) {
   Tile x;
-  const int64_t nf = static_cast<int64_t>(g.nfull) * g.tiles_full;
-  if (i < nf) {
-    x.rl = static_cast<int32_t>(i / g.tiles_full);
-    x.t = i - static_cast<int64_t>(x.rl) * g.tiles_full;
-    x.len = g.S;
-    x.tiles = g.tiles_full;
-  } else {
-    x.rl = g.nfull;
-    x.t = i - nf;
-    x.len = g.len_part;
-    x.tiles = g.tiles_part;
-  }
+  x.rl = rl;
+  x.t = t;
+  x.sidx = static_cast<int64_t>(rl) * g.tiles_full + t;
+  const bool full = rl < g.nfull;
+  x.len = full ? g.S : g.len_part;
+  x.tiles = full ? g.tiles_full : g.tiles_part;
   x.nb = (x.len + g.B - 1) / g.B;
   x.k0 = x.t * g.T;
   const int64_t nblk = x.nb - x.k0 < g.T ? x.nb - x.k0 : g.T;
@@ -202,6 +206,28 @@ __device__ __forceinline__ Tile decode_tile(const Geometry& g, int64_t i) {
   x.te = te < nblk * g.B ? te : nblk * g.B;
   x.shard_off = static_cast<int64_t>(x.rl) * g.S;
   return x;
+}
+
+// Shard-major order: tile i of the range (used where tiles are independent).
+__device__ __forceinline__ Tile decode_tile(const Geometry& g, int64_t i) {
+  const int64_t nf = static_cast<int64_t>(g.nfull) * g.tiles_full;
+  if (i < nf) {
+    const int32_t rl = static_cast<int32_t>(i / g.tiles_full);
+    return make_tile(g, rl, i - static_cast<int64_t>(rl) * g.tiles_full);
+  }
+  return make_tile(g, g.nfull, i - nf);
+}
+
+// Interleaved order of the compress tickets: tile t of every shard, then
+// tile t+1 of every shard, ...  Each shard's look-back chain then advances
+// by one tile every R tickets instead of every ticket, and tiles of one
+// shard still start in order (tile t always before tile t+1).
+__device__ __forceinline__ Tile decode_ticket(const Geometry& g, int64_t i) {
+  const int64_t P = g.nfull + g.has_part;  // shards with tiles
+  const int64_t head = g.tiles_part * P;   // rows in which the partial shard takes part
+  if (i < head) return make_tile(g, static_cast<int32_t>(i % P), i / P);
+  const int64_t j = i - head;
+  return make_tile(g, static_cast<int32_t>(j % g.nfull), g.tiles_part + j / g.nfull);
 }
 
 __device__ __forceinline__ int64_t shard_len_of(const Geometry& g, int32_t rl) {
@@ -223,27 +249,32 @@ __device__ __forceinline__ bool flag_of(const uint32_t* fw, int kb) {
 }
 
 // ------------------------------------------------------------------------
-// Decoupled look-back over the per-tile count of changed blocks (warp 0).
-// Publishes this tile's aggregate, sums predecessors' aggregates until an
-// inclusive prefix is found, publishes the inclusive prefix and returns the
-// exclusive one (clamped to k0 so that every offset stays in bounds even
-// after a timeout).
+// Decoupled look-back over the per-tile count of changed blocks.
 
-__device__ uint32_t lookback(const CompressParams& p, int64_t g, const Tile& x, uint32_t agg,
-                             uint32_t lane, bool* timed_out) {
-  unsigned long long* st = p.tile_status;
-  const unsigned long long ep = static_cast<unsigned long long>(p.epoch) << 32;
-  const unsigned long long incl = static_cast<unsigned long long>(kStateInclusive) << 30;
-  const unsigned long long aggr = static_cast<unsigned long long>(kStateAggregate) << 30;
-  const bool skip_publish = (p.flags & CIERA_DEBUG_SKIP_FIRST_PUBLISH) && x.t == 0;
+__device__ __forceinline__ void publish(const CompressParams& p, const Tile& x, uint32_t state,
+                                        uint32_t value) {
+  const unsigned long long v = (static_cast<unsigned long long>(p.epoch) << 32) |
+                               (static_cast<unsigned long long>(state) << 30) | value;
+  st_release_u64(&p.tile_status[x.sidx], v);
+}
+
+// Warp-wide: the number of changed blocks in the tiles before x in its
+// shard.  Reads 32 predecessors per round and sums their aggregates until
+// one of them carries an inclusive prefix.  It needs nothing of tile x
+// itself, so it runs while x's own values are still being copied in.  The
+// result is clamped to k0 so that every offset stays in bounds even after a
+// timeout.
+__device__ uint32_t lookback_exclusive(const CompressParams& p, const Tile& x, uint32_t lane,
+                                       bool* timed_out) {
   if (x.t == 0) {
-    if (lane == 0 && !skip_publish) st_release_u64(&st[g], ep | incl | agg);
+    *timed_out = false;
     return 0;
   }
-  if (lane == 0) st_release_u64(&st[g], ep | aggr | agg);
-
-  const int64_t gfirst = g - x.t;
-  int64_t base = g - 1;
+  const unsigned long long* st = p.tile_status;
+  const unsigned long long ep = static_cast<unsigned long long>(p.epoch) << 32;
+  const unsigned long long incl = static_cast<unsigned long long>(kStateInclusive) << 30;
+  const int64_t gfirst = x.sidx - x.t;
+  int64_t base = x.sidx - 1;
   uint32_t X = 0;
   bool to = false;
   uint64_t t0 = 0;
@@ -283,67 +314,78 @@ __device__ uint32_t lookback(const CompressParams& p, int64_t g, const Tile& x, 
     base -= 32;
   }
   if (X > static_cast<uint64_t>(x.k0)) X = static_cast<uint32_t>(x.k0);
-  if (lane == 0) st_release_u64(&st[g], ep | incl | (X + agg));
   *timed_out = __any_sync(0xffffffffu, to);
   return X;
 }
 
 // ------------------------------------------------------------------------
-// Compress: shared state of one CTA
+// Compress: one CTA per tile, tiles in ticket order.
+//
+//   thread 0   draws the ticket, starts the bulk copies of the tile's
+//              values and cached exponents into shared memory
+//   warp 0     meanwhile walks the look-back for the tile's exclusive prefix
+//   warps 1-3  wait for the copies, flag the tile's blocks, write the flag
+//              bytes and publish the tile's aggregate
+//   then       warp 0 publishes the inclusive prefix, all warps pack, thread
+//              0 issues the bulk stores of the body, and the shard's last
+//              tile writes the descriptor and the bitmap.
+// Dynamic shared memory: fw[W] flag words | fpre[W] their exclusive
+// popcount prefix | (staged tiles) ws[2*TE] values | cs[TE] cached exponents.
 
 struct CompressShared {
-  uint32_t ticket_lo, ticket_hi;
-  uint32_t X;
-  uint32_t agg;
-  uint32_t bad;  // a bounded wait ran out
-  uint32_t fw[kMaxTileWords + 1];    // flag bits of the tile's blocks
-  uint32_t fpre[kMaxTileWords + 1];  // exclusive popcount prefix of fw
+  uint32_t ticket;
+  uint32_t X;     // changed blocks before the tile in its shard
+  uint32_t agg;   // changed blocks in the tile
+  uint32_t bad;   // a bounded wait ran out on this tile
 };
 
 __device__ __forceinline__ void record_status(Control* ctl, uint32_t bits) {
   atomicOr(&ctl->status, bits);
 }
 
-// Flag bytes, aggregate, look-back; leaves sh.X and sh.fpre ready.
-__device__ void compress_publish(const CompressParams& p, int64_t g, const Tile& x,
-                                 CompressShared& sh) {
-  const int tid = threadIdx.x;
+// Named barrier of the 96 flagging threads (warps 1-3).
+__device__ __forceinline__ void flaggers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 32) : "memory");
+}
+
+// Warps 1-3, after the flag bits are final: flag bytes, popcount prefix,
+// aggregate, and its publication (the inclusive prefix directly for a
+// shard's first tile).
+__device__ void publish_aggregate(const CompressParams& p, const Tile& x, const CompressShared& s0,
+                                  CompressShared& sh, uint32_t* fw, uint32_t* fpre) {
+  const int ft = threadIdx.x - 32;  // 0..95
   const int nw = (x.nblk + 31) >> 5;
   uint8_t* fb = p.flagbytes + static_cast<int64_t>(x.rl) * p.flag_stride + x.k0;
-  for (int kb = tid; kb < x.nblk; kb += blockDim.x) fb[kb] = flag_of(sh.fw, kb) ? 1 : 0;
-  if (tid == 0) {
+  if (x.nblk > 32) {
+    for (int kb = ft; kb < x.nblk; kb += kThreads - 32) fb[kb] = flag_of(fw, kb) ? 1 : 0;
+    if (ft < x.nblk) __threadfence();
+    flaggers_sync();
+  }
+  if (ft == 0) {
+    // the release of the status below orders these writes (and, through
+    // the fences above, those of the other flagging threads)
+    if (x.nblk <= 32)
+      for (int kb = 0; kb < x.nblk; ++kb) fb[kb] = flag_of(fw, kb) ? 1 : 0;
     uint32_t run = 0;
     for (int i = 0; i < nw; ++i) {
-      sh.fpre[i] = run;
-      run += __popc(sh.fw[i]);
+      fpre[i] = run;
+      run += __popc(fw[i]);
     }
     sh.agg = run;
+    const bool skip = (p.flags & CIERA_DEBUG_SKIP_FIRST_PUBLISH) && x.t == 0;
+    if (!skip) publish(p, x, x.t == 0 ? kStateInclusive : kStateAggregate, run);
   }
-  __threadfence();
-  __syncthreads();
-  if (tid < 32) {
-    bool to = false;
-    const uint32_t X = lookback(p, g, x, sh.agg, tid, &to);
-    if (tid == 0) {
-      sh.X = X;
-      if (to) {
-        sh.bad = 1;
-        record_status(p.ctl, kStatusTimeout);
-      }
-    }
-    __threadfence();
-  }
-  __syncthreads();
+  (void)s0;
 }
 
 // Last tile of a shard: descriptor and bitmap.
-__device__ void compress_epilogue(const CompressParams& p, const Tile& x,
-                                  const CompressShared& sh) {
+__device__ void compress_epilogue(const CompressParams& p, const Tile& x, const CompressShared& sh,
+                                  const uint32_t* fw) {
   const int tid = threadIdx.x;
   const int64_t B = p.geo.B;
   const uint32_t total = sh.X + sh.agg;  // changed blocks in the shard
   const int64_t last_len = x.len - (x.nb - 1) * B;
-  const bool last_changed = flag_of(sh.fw, static_cast<int>(x.nb - 1 - x.k0));
+  const bool last_changed = flag_of(fw, static_cast<int>(x.nb - 1 - x.k0));
   const int64_t changed_vals =
       static_cast<int64_t>(total) * B - (last_changed ? (B - last_len) : 0);
   const int64_t body = x.len + changed_vals;
@@ -359,150 +401,18 @@ __device__ void compress_epilogue(const CompressParams& p, const Tile& x,
     p.descs[x.rl] = d;
   }
   if (!raw) {
-    // every earlier tile wrote its flag bytes before publishing; the
-    // look-back's acquire chain makes them visible here
+    // every earlier tile wrote its flag bytes before publishing its status;
+    // read them from L2 (other CTAs wrote them during this launch)
     const uint8_t* fb = p.flagbytes + static_cast<int64_t>(x.rl) * p.flag_stride;
     for (int64_t i = tid; i < bm; i += blockDim.x) {
       uint32_t byte = 0;
       for (int j = 0; j < 8; ++j) {
         const int64_t k = 8 * i + j;
-        if (k < x.nb) byte |= static_cast<uint32_t>(fb[k] & 1u) << j;
+        if (k < x.nb) byte |= static_cast<uint32_t>(__ldcg(fb + k) & 1u) << j;
       }
       payload[body + i] = static_cast<uint8_t>(byte);
     }
   }
-}
-
-// Byte-wise tile: any block size, any alignment.
-__device__ void compress_tile_bytes(const CompressParams& p, int64_t g, const Tile& x,
-                                    CompressShared& sh) {
-  const int tid = threadIdx.x;
-  const int64_t B = p.geo.B;
-  const uint16_t* w = p.w + x.shard_off + x.e0;
-  uint8_t* c = p.scache + x.shard_off + x.e0;
-  if (p.flags & CIERA_COLD) {
-    for (int kb = tid; kb < x.nblk; kb += blockDim.x) atomicOr(&sh.fw[kb >> 5], 1u << (kb & 31));
-  } else {
-    for (int64_t j = tid; j < x.te; j += blockDim.x) {
-      if (exp1(w[j]) != c[j]) {
-        const int kb = static_cast<int>(j / B);
-        atomicOr(&sh.fw[kb >> 5], 1u << (kb & 31));
-      }
-    }
-  }
-  __syncthreads();
-  compress_publish(p, g, x, sh);
-  uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
-  for (int64_t j = tid; j < x.te; j += blockDim.x) {
-    const int kb = static_cast<int>(j / B);
-    const int64_t within = j - kb * B;
-    const int64_t kg = x.k0 + kb;
-    const int64_t off = (kg + sh.X + count_before(sh.fw, sh.fpre, kb)) * B;
-    const uint32_t v = w[j];
-    if (flag_of(sh.fw, kb)) {
-      payload[off + 2 * within] = static_cast<uint8_t>(v & 0xFFu);
-      payload[off + 2 * within + 1] = static_cast<uint8_t>(v >> 8);
-      const uint8_t e = static_cast<uint8_t>(exp1(v));
-      if (c[j] != e) c[j] = e;
-    } else {
-      payload[off + within] = static_cast<uint8_t>(sm1(v));
-    }
-  }
-  __syncthreads();
-  if (x.t == x.tiles - 1) compress_epilogue(p, x, sh);
-}
-
-// Staged tile: T*B values, a multiple of 16, 16-byte aligned everywhere.
-// Shared memory: ws[2*TE] values | cs[TE] cached exponents | os[TE] sm bytes.
-__device__ void compress_tile_staged(const CompressParams& p, int64_t g, const Tile& x,
-                                     CompressShared& sh, uint8_t* dsm, uint64_t* bar) {
-  const int tid = threadIdx.x;
-  const int64_t B = p.geo.B;
-  const int64_t TE = p.geo.T * B;
-  uint8_t* ws = dsm;
-  uint8_t* cs = dsm + 2 * TE;
-  uint8_t* os = dsm + 3 * TE;
-  const uint16_t* w = p.w + x.shard_off + x.e0;
-  uint8_t* c = p.scache + x.shard_off + x.e0;
-  const uint32_t te = static_cast<uint32_t>(x.te);
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_barrier_init();
-    mbar_arrive_expect_tx(bar, 3u * te);
-    bulk_g2s(ws, w, 2u * te, bar);
-    bulk_g2s(cs, c, te, bar);
-  }
-  __syncthreads();
-  const bool ok = mbar_wait_bounded(bar, 0, p.timeout_ns);
-  if (__syncthreads_or(!ok)) {
-    // the copies did not land in time: record it, wait once more for them
-    // so that no copy is left writing into this CTA's shared memory
-    if (tid == 0) {
-      record_status(p.ctl, kStatusTimeout);
-      sh.bad = 1;
-    }
-    mbar_wait_bounded(bar, 0, p.timeout_ns);
-    __syncthreads();
-  }
-  const int ngroups = static_cast<int>(te >> 4);
-  const bool cold = p.flags & CIERA_COLD;
-  if (cold || sh.bad) {
-    for (int kb = tid; kb < x.nblk; kb += blockDim.x) atomicOr(&sh.fw[kb >> 5], 1u << (kb & 31));
-  } else {
-    for (int gi = tid; gi < ngroups; gi += blockDim.x) {
-      const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
-      const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
-      const uint4 cc = reinterpret_cast<const uint4*>(cs)[gi];
-      const uint32_t d = (exp4(w0.x, w0.y) ^ cc.x) | (exp4(w0.z, w0.w) ^ cc.y) |
-                         (exp4(w1.x, w1.y) ^ cc.z) | (exp4(w1.z, w1.w) ^ cc.w);
-      if (d) {
-        const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
-        atomicOr(&sh.fw[kb >> 5], 1u << (kb & 31));
-      }
-    }
-  }
-  __syncthreads();
-  compress_publish(p, g, x, sh);
-
-  // pack: sign+mantissa bytes of unchanged blocks into os; exponents of
-  // changed blocks into the sender cache (only the 16-byte groups that differ)
-  for (int gi = tid; gi < ngroups; gi += blockDim.x) {
-    const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
-    const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
-    const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
-    if (flag_of(sh.fw, kb)) {
-      const uint4 e = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w), exp4(w1.x, w1.y),
-                                 exp4(w1.z, w1.w));
-      const uint4 cc = reinterpret_cast<const uint4*>(cs)[gi];
-      if (cold || ((e.x ^ cc.x) | (e.y ^ cc.y) | (e.z ^ cc.z) | (e.w ^ cc.w)))
-        reinterpret_cast<uint4*>(c)[gi] = e;
-    } else {
-      reinterpret_cast<uint4*>(os)[gi] =
-          make_uint4(sm4(w0.x, w0.y), sm4(w0.z, w0.w), sm4(w1.x, w1.y), sm4(w1.z, w1.w));
-    }
-  }
-  fence_proxy_async_smem();
-  __syncthreads();
-  if (tid == 0) {
-    uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
-    int ka = 0;
-    while (ka < x.nblk) {
-      const bool f = flag_of(sh.fw, ka);
-      int kz = ka + 1;
-      while (kz < x.nblk && flag_of(sh.fw, kz) == f) ++kz;
-      const int64_t ea = static_cast<int64_t>(ka) * B;
-      const int64_t ez = static_cast<int64_t>(kz) * B < x.te ? static_cast<int64_t>(kz) * B : x.te;
-      const int64_t off = (x.k0 + ka + sh.X + count_before(sh.fw, sh.fpre, ka)) * B;
-      if (f)
-        bulk_s2g(payload + off, ws + 2 * ea, static_cast<uint32_t>(2 * (ez - ea)));
-      else
-        bulk_s2g(payload + off, os + ea, static_cast<uint32_t>(ez - ea));
-      ka = kz;
-    }
-    bulk_commit();
-  }
-  if (x.t == x.tiles - 1) compress_epilogue(p, x, sh);
-  if (tid == 0) bulk_wait_read_all();
 }
 
 __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
@@ -510,17 +420,33 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
   __shared__ CompressShared sh;
   __shared__ __align__(8) uint64_t bar;
   const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int64_t B = p.geo.B;
+  const int64_t TE = p.geo.T * B;
+  const int W = static_cast<int>((p.geo.T + 31) / 32);
+  uint32_t* fw = reinterpret_cast<uint32_t*>(dsm);
+  uint32_t* fpre = fw + W;
+  uint8_t* ws = dsm + ((8 * W + 127) & ~127);
+  uint8_t* cs = ws + 2 * TE;
+
   if (tid == 0) {
     // ticket order = start order: a tile only ever waits on tiles whose
-    // CTAs started earlier, so the look-back cannot wait on an unscheduled CTA
+    // CTAs started earlier, so the look-back never waits on an unscheduled CTA
     const uint32_t t = atomicAdd(&p.ctl->ticket, 1u);
     if (t == gridDim.x - 1) atomicExch(&p.ctl->ticket, 0u);
-    sh.ticket_lo = t;
+    sh.ticket = t;
     sh.bad = 0;
   }
-  for (int i = tid; i <= kMaxTileWords; i += blockDim.x) sh.fw[i] = 0;
+  // the launch must provide the flag words (and the staging of staged
+  // tiles); if it does not, report it instead of touching memory past it
+  const uint32_t need = static_cast<uint32_t>(((8 * W + 127) & ~127) + (p.fast ? 3 * TE : 0));
+  if (dynamic_smem_size() < need) {
+    if (tid == 0) record_status(p.ctl, kStatusInternal);
+    return;
+  }
+  for (int i = tid; i < W; i += blockDim.x) fw[i] = 0;
   __syncthreads();
-  const int64_t g = sh.ticket_lo;
+  const int64_t g = sh.ticket;
   if (g >= p.geo.total_tiles) {
     // the last ticket: descriptors of empty shards in the range
     for (int32_t rl = p.geo.nfull + p.geo.has_part + tid; rl < p.geo.rank_count;
@@ -534,11 +460,133 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
     }
     return;
   }
-  const Tile x = decode_tile(p.geo, g);
-  if (p.fast && (x.te & 15) == 0)
-    compress_tile_staged(p, g, x, sh, dsm, &bar);
-  else
-    compress_tile_bytes(p, g, x, sh);
+  const Tile x = decode_ticket(p.geo, g);
+  const bool stg = p.fast && (x.te & 15) == 0;
+  const bool cold = p.flags & CIERA_COLD;
+  const uint16_t* w = p.w + x.shard_off + x.e0;
+  uint8_t* c = p.scache + x.shard_off + x.e0;
+  const uint32_t te = static_cast<uint32_t>(x.te);
+  if (stg && tid == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(&bar, 3u * te);
+    bulk_g2s(ws, w, 2u * te, &bar);
+    bulk_g2s(cs, c, te, &bar);
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    bool to = false;
+    const uint32_t X = lookback_exclusive(p, x, lane, &to);
+    if (lane == 0) {
+      sh.X = X;
+      if (to) record_status(p.ctl, kStatusTimeout);
+    }
+    // the shard's last tile reads every other tile's flag bytes later on
+    if (x.t == x.tiles - 1) __threadfence();
+    if (stg) mbar_wait_bounded(&bar, 0, p.timeout_ns);  // this warp reads ws/cs too
+  } else {
+    const int ft = tid - 32;
+    if (stg) {
+      if (!mbar_wait_bounded(&bar, 0, p.timeout_ns)) {
+        // record it and wait once more, so no copy still writes into this
+        // CTA's shared memory when it exits
+        record_status(p.ctl, kStatusTimeout);
+        sh.bad = 1;
+        mbar_wait_bounded(&bar, 0, p.timeout_ns);
+      }
+    }
+    flaggers_sync();
+    if (cold || sh.bad) {
+      for (int kb = ft; kb < x.nblk; kb += kThreads - 32) atomicOr(&fw[kb >> 5], 1u << (kb & 31));
+    } else if (stg) {
+      const int ngroups = static_cast<int>(te >> 4);
+      for (int gi = ft; gi < ngroups; gi += kThreads - 32) {
+        const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
+        const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
+        const uint4 cc = reinterpret_cast<const uint4*>(cs)[gi];
+        const uint32_t d = (exp4(w0.x, w0.y) ^ cc.x) | (exp4(w0.z, w0.w) ^ cc.y) |
+                           (exp4(w1.x, w1.y) ^ cc.z) | (exp4(w1.z, w1.w) ^ cc.w);
+        if (d) {
+          const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
+          atomicOr(&fw[kb >> 5], 1u << (kb & 31));
+        }
+      }
+    } else {
+      for (int64_t j = ft; j < x.te; j += kThreads - 32) {
+        if (exp1(w[j]) != c[j]) {
+          const int kb = static_cast<int>(j / B);
+          atomicOr(&fw[kb >> 5], 1u << (kb & 31));
+        }
+      }
+    }
+    flaggers_sync();
+    publish_aggregate(p, x, sh, sh, fw, fpre);
+  }
+  __syncthreads();
+  if (tid == 0 && x.t > 0) publish(p, x, kStateInclusive, sh.X + sh.agg);
+
+  uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
+  if (stg) {
+    // Sign+mantissa bytes of an unchanged block overwrite its own cached
+    // exponents in cs (a group either reads cs -- changed block -- or writes
+    // it -- unchanged block -- never both).  Changed blocks refresh the
+    // sender cache, writing only the 16-byte groups that differ.
+    const int ngroups = static_cast<int>(te >> 4);
+    for (int gi = tid; gi < ngroups; gi += blockDim.x) {
+      const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
+      const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
+      const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
+      if (flag_of(fw, kb)) {
+        const uint4 e = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w), exp4(w1.x, w1.y),
+                                   exp4(w1.z, w1.w));
+        const uint4 cc = reinterpret_cast<const uint4*>(cs)[gi];
+        if (cold || ((e.x ^ cc.x) | (e.y ^ cc.y) | (e.z ^ cc.z) | (e.w ^ cc.w)))
+          reinterpret_cast<uint4*>(c)[gi] = e;
+      } else {
+        reinterpret_cast<uint4*>(cs)[gi] =
+            make_uint4(sm4(w0.x, w0.y), sm4(w0.z, w0.w), sm4(w1.x, w1.y), sm4(w1.z, w1.w));
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      int ka = 0;
+      while (ka < x.nblk) {
+        const bool f = flag_of(fw, ka);
+        int kz = ka + 1;
+        while (kz < x.nblk && flag_of(fw, kz) == f) ++kz;
+        const int64_t ea = static_cast<int64_t>(ka) * B;
+        const int64_t ez =
+            static_cast<int64_t>(kz) * B < x.te ? static_cast<int64_t>(kz) * B : x.te;
+        const int64_t off = (x.k0 + ka + sh.X + count_before(fw, fpre, ka)) * B;
+        if (f)
+          bulk_s2g(payload + off, ws + 2 * ea, static_cast<uint32_t>(2 * (ez - ea)));
+        else
+          bulk_s2g(payload + off, cs + ea, static_cast<uint32_t>(ez - ea));
+        ka = kz;
+      }
+      bulk_commit();
+    }
+  } else {
+    for (int64_t j = tid; j < x.te; j += blockDim.x) {
+      const int kb = static_cast<int>(j / B);
+      const int64_t within = j - kb * B;
+      const int64_t kg = x.k0 + kb;
+      const int64_t off = (kg + sh.X + count_before(fw, fpre, kb)) * B;
+      const uint32_t v = w[j];
+      if (flag_of(fw, kb)) {
+        payload[off + 2 * within] = static_cast<uint8_t>(v & 0xFFu);
+        payload[off + 2 * within + 1] = static_cast<uint8_t>(v >> 8);
+        const uint8_t e = static_cast<uint8_t>(exp1(v));
+        if (c[j] != e) c[j] = e;
+      } else {
+        payload[off + within] = static_cast<uint8_t>(sm1(v));
+      }
+    }
+  }
+  if (x.t == x.tiles - 1) compress_epilogue(p, x, sh, fw);
+  if (stg && tid == 0) bulk_wait_read_all();
 }
 
 // A raw payload whose body was written in compressed layout (possible only
@@ -649,7 +697,7 @@ __global__ void __launch_bounds__(kScanThreads) k_bitmap_scan(const DecompressPa
 struct DecompressShared {
   uint32_t X;
   uint32_t bad;
-  uint32_t fw[2];  // flag bits of the tile's blocks (staged path: T <= 16)
+  uint32_t fw[2];  // flag bits of the tile's blocks (staged path: T <= 32)
 };
 
 // Byte-wise tile of the receiver.
@@ -710,7 +758,7 @@ __device__ void decompress_tile_staged(const DecompressParams& p, const Tile& x,
       mbar_arrive_expect_tx(bar, 2u * te);
       bulk_g2s(ws, payload + 2 * x.e0, 2u * te, bar);
     } else {
-      // flag bits of blocks k0 .. k0+nblk-1 (nblk <= 16, may straddle a word)
+      // flag bits of blocks k0 .. k0+nblk-1 (nblk <= 32, may straddle a word)
       const uint32_t* words = p.bm_words + static_cast<int64_t>(x.rl) * p.nw_stride;
       const uint32_t* pre = p.bm_prefix + static_cast<int64_t>(x.rl) * p.nw_stride;
       const int64_t wi = x.k0 >> 5;
@@ -789,6 +837,10 @@ __global__ void __launch_bounds__(kThreads) k_decompress(const DecompressParams 
   __shared__ DecompressShared sh;
   __shared__ __align__(8) uint64_t bar;
   const Tile x = decode_tile(p.geo, blockIdx.x);
+  if (p.fast && dynamic_smem_size() < static_cast<uint32_t>(4 * p.geo.T * p.geo.B)) {
+    if (threadIdx.x == 0) atomicOr(&p.ctl->status, kStatusInternal);
+    return;
+  }
   const uint32_t state = p.rank_state[x.rl];
   if (state == kRankSkip) return;
   if (p.fast && (x.te & 15) == 0)
@@ -797,18 +849,40 @@ __global__ void __launch_bounds__(kThreads) k_decompress(const DecompressParams 
     decompress_tile_bytes(p, x, state);
 }
 
+// Largest dynamic shared memory already allowed per device and kernel.
+constexpr int kMaxDevices = 64;
+std::atomic<int64_t> g_compress_smem[kMaxDevices];
+std::atomic<int64_t> g_decompress_smem[kMaxDevices];
+
+// Opt the kernel in to `bytes` of dynamic shared memory on the current
+// device (the default limit, static + dynamic, is 48 KB).
+cudaError_t allow_dynamic_smem(const void* fn, int64_t bytes, std::atomic<int64_t>* done) {
+  if (bytes <= 0) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < kMaxDevices && done[dev].load(std::memory_order_relaxed) >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(bytes));
+  if (e == cudaSuccess && dev < kMaxDevices) {
+    int64_t cur = done[dev].load(std::memory_order_relaxed);
+    while (cur < bytes && !done[dev].compare_exchange_weak(cur, bytes)) {
+    }
+  }
+  return e;
+}
+
 }  // namespace
 
 int launch_compress(const CompressParams& p, int64_t smem_bytes, int raw_fixup, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (smem_bytes > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k_compress, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes));
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(k_compress), smem_bytes,
+                                     g_compress_smem);
+  if (e != cudaSuccess) return e;
+  // one CTA per tile, plus the last ticket (descriptors of empty shards)
   const int64_t grid = p.geo.total_tiles + 1;
   k_compress<<<static_cast<unsigned>(grid), kThreads, static_cast<size_t>(smem_bytes), s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (raw_fixup && p.geo.total_tiles > 0) {
     k_raw_fixup<<<static_cast<unsigned>(p.geo.total_tiles), kThreads, 0, s>>>(p);
@@ -819,14 +893,12 @@ int launch_compress(const CompressParams& p, int64_t smem_bytes, int raw_fixup, 
 
 int launch_decompress(const DecompressParams& p, int64_t smem_bytes, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (smem_bytes > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(
-        k_decompress, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(k_decompress), smem_bytes,
+                                     g_decompress_smem);
+  if (e != cudaSuccess) return e;
   if (p.geo.rank_count > 0) {
     k_bitmap_scan<<<static_cast<unsigned>(p.geo.rank_count), kScanThreads, 0, s>>>(p);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (p.geo.total_tiles > 0) {

@@ -108,6 +108,8 @@ def workload(cfg: int, variant: str = "") -> Workload:
        steps 2.2e-6 / 2.35e-5 / 3.9e-4
     variant "clustered<p>" (cfg 2 or 5): each block is perturbed with
     probability p and left untouched otherwise.
+    variant "experts<k>" (cfg 2, 3 or 5): the same layer cut to its first k
+    experts (a smaller case of the same kernels, e.g. for profiling).
     """
     if cfg == 1:
         w = Workload("cfg1_matrix_256x512", (Tensor("w", (256, 512)),), 1, 4, 256, 3,
@@ -125,11 +127,15 @@ def workload(cfg: int, variant: str = "") -> Workload:
                      4096, 16, (2.2e-6,) * 5 + (2.35e-5,) * 5 + (3.9e-4,) * 5)
     else:
         raise ValueError(f"no workload {cfg}")
-    if variant:
-        if not variant.startswith("clustered"):
-            raise ValueError(f"unknown variant {variant!r}")
-        p = float(variant[len("clustered"):])
-        w = dataclasses.replace(w, name=f"{w.name}_clustered{p:g}", p_block=p)
+    for v in filter(None, variant.split(",")):
+        if v.startswith("clustered"):
+            p = float(v[len("clustered"):])
+            w = dataclasses.replace(w, name=f"{w.name}_clustered{p:g}", p_block=p)
+        elif v.startswith("experts") and cfg in (2, 3, 5):
+            k = int(v[len("experts"):])
+            w = dataclasses.replace(w, name=f"{w.name}_experts{k}", tensors=w.tensors[:3 * k])
+        else:
+            raise ValueError(f"unknown variant {v!r}")
     return w
 
 

@@ -37,12 +37,12 @@ def test_library_exports_every_declared_symbol():
 def test_plan_geometry():
     p = ciera.Plan((256, 512), 256, 4)
     i = p.info
-    assert (i.numel, i.shard_len, i.blocks_per_shard, i.tile_blocks) == (131072, 32768, 128, 16)
-    assert i.total_tiles == 4 * 8 and i.fast_path and not i.raw_fixup
+    assert (i.numel, i.shard_len, i.blocks_per_shard, i.tile_blocks) == (131072, 32768, 128, 32)
+    assert i.total_tiles == 4 * 4 and i.fast_path and not i.raw_fixup
     assert i.payload_capacity >= 2 * i.shard_len and i.payload_capacity % 256 == 0
     p = ciera.Plan(402653184, 4096, 16)
-    assert (p.info.shard_len, p.info.blocks_per_shard, p.info.total_tiles) == (
-        25165824, 6144, 98304)
+    assert (p.info.shard_len, p.info.blocks_per_shard, p.info.tile_blocks,
+            p.info.total_tiles) == (25165824, 6144, 2, 49152)
     # ragged: 10 values over 4 ranks -> 3,3,3,1
     p = ciera.Plan(10, 2, 4)
     assert p.info.shard_len == 3 and not p.info.fast_path
