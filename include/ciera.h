@@ -168,6 +168,30 @@ int ciera_decompress(ciera_plan_t plan, const uint8_t *payloads_dev, int64_t pay
  * CIERA_E_CUDA. */
 int ciera_status(void *workspace_dev, void *stream);
 
+/* Sender side without a workspace, for callers that cannot allocate device
+ * memory where they compress (inside a communication hook or an allocator
+ * callback, where allocating would re-enter the allocator; or C callers with
+ * no device allocator of their own).  The paper has no counterpart: this is
+ * ciera_compress with the same arguments and results, except that its
+ * scratch (ticket counter, status word, look-back words, flag bytes) lives
+ * in a fixed 4 MiB device array inside the library, which every GPU that
+ * loads the library holds until the process exits.
+ *   status_dev  optional (may be NULL): one device word the call sets to 0
+ *               when its kernel finished normally, nonzero when a bounded
+ *               wait ran out or the launch was inconsistent (the payloads of
+ *               that call are then not valid)
+ * It allocates nothing (no cudaMalloc, no allocating library routine).  Its
+ * first call on a device looks up the array's device address; make that
+ * first call before any stream capture.  Every call shares the one array:
+ * calls that can overlap on the GPU (other streams, other host threads)
+ * race and must be serialised by the caller.
+ * Errors: CIERA_E_INVAL as ciera_compress, and for a plan whose
+ * info.workspace_bytes exceeds 4 MiB; CIERA_E_CUDA. */
+int ciera_compress_noalloc(ciera_plan_t plan, int rank_begin, int rank_count,
+                           const uint16_t *w_dev, uint8_t *sender_cache_dev, uint8_t *payloads_dev,
+                           int64_t payload_stride, ciera_desc *descs_dev, uint8_t *flags_dev,
+                           uint32_t *status_dev, uint32_t flags, void *stream);
+
 /* Per-tensor predicate (Section 3.2): 1 = compress, 0 = send raw.
  * With P = N + q*N + ceil(ceil(N/B)/8) expected payload bytes,
  * compress iff (2N - P)/link_Bps > t_fixed_s + (4 + q)*N/hbm_Bps. */

@@ -66,6 +66,8 @@ SIGNATURES = {
     "ciera_workspace_init": (_i32, [_vp, _vp, _vp]),
     "ciera_compress": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _u32, _vp]),
     "ciera_decompress": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _u32, _vp]),
+    "ciera_compress_noalloc": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _u32,
+                                      _vp]),
     "ciera_status": (_i32, [_vp, _vp]),
     "ciera_should_compress": (_i32, [_i64]),
     "ciera_set_cost_model": (_i32, [ctypes.POINTER(_CostModel)]),
