@@ -10,8 +10,11 @@ namespace ciera {
 
 constexpr int kThreads = 128;             // threads per CTA of the tile kernels
 constexpr int kScanThreads = 256;         // threads per CTA of the bitmap scan
-constexpr int64_t kTileElems = 8192;      // target values per tile (T*B)
-constexpr int kMaxTileBlocks = 8192;      // T <= 8192 (B = 1)
+#ifndef CIERA_TILE_ELEMS
+#define CIERA_TILE_ELEMS 8192
+#endif
+constexpr int64_t kTileElems = CIERA_TILE_ELEMS;  // target values per tile (T*B)
+constexpr int kMaxTileBlocks = static_cast<int>(kTileElems);  // T <= kTileElems (B = 1)
 constexpr int kMaxTileWords = kMaxTileBlocks / 32;
 constexpr int64_t kFastMinBlock = 256;    // fast path: T <= 32 blocks per tile
 constexpr int64_t kFastMaxBlock = 16384;  // fast path: <= 64 KB of staging per CTA

@@ -522,34 +522,38 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
     }
     flaggers_sync();
     publish_aggregate(p, x, sh, sh, fw, fpre);
+    if (stg) {
+      // Pack while warp 0 may still be looking back: nothing here depends
+      // on the prefix.  Sign+mantissa bytes of an unchanged block overwrite
+      // its own cached exponents in cs (a group either reads cs -- changed
+      // block -- or writes it -- unchanged block -- never both).  Changed
+      // blocks refresh the sender cache, writing only the 16-byte groups
+      // that differ.
+      const int ngroups = static_cast<int>(te >> 4);
+      for (int gi = ft; gi < ngroups; gi += kThreads - 32) {
+        const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
+        const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
+        const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
+        if (flag_of(fw, kb)) {
+          const uint4 e = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w), exp4(w1.x, w1.y),
+                                     exp4(w1.z, w1.w));
+          const uint4 cc = reinterpret_cast<const uint4*>(cs)[gi];
+          if (cold || ((e.x ^ cc.x) | (e.y ^ cc.y) | (e.z ^ cc.z) | (e.w ^ cc.w)))
+            reinterpret_cast<uint4*>(c)[gi] = e;
+        } else {
+          reinterpret_cast<uint4*>(cs)[gi] =
+              make_uint4(sm4(w0.x, w0.y), sm4(w0.z, w0.w), sm4(w1.x, w1.y), sm4(w1.z, w1.w));
+        }
+      }
+      fence_proxy_async_smem();
+    }
   }
   __syncthreads();
   if (tid == 0 && x.t > 0) publish(p, x, kStateInclusive, sh.X + sh.agg);
 
   uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
   if (stg) {
-    // Sign+mantissa bytes of an unchanged block overwrite its own cached
-    // exponents in cs (a group either reads cs -- changed block -- or writes
-    // it -- unchanged block -- never both).  Changed blocks refresh the
-    // sender cache, writing only the 16-byte groups that differ.
-    const int ngroups = static_cast<int>(te >> 4);
-    for (int gi = tid; gi < ngroups; gi += blockDim.x) {
-      const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
-      const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
-      const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
-      if (flag_of(fw, kb)) {
-        const uint4 e = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w), exp4(w1.x, w1.y),
-                                   exp4(w1.z, w1.w));
-        const uint4 cc = reinterpret_cast<const uint4*>(cs)[gi];
-        if (cold || ((e.x ^ cc.x) | (e.y ^ cc.y) | (e.z ^ cc.z) | (e.w ^ cc.w)))
-          reinterpret_cast<uint4*>(c)[gi] = e;
-      } else {
-        reinterpret_cast<uint4*>(cs)[gi] =
-            make_uint4(sm4(w0.x, w0.y), sm4(w0.z, w0.w), sm4(w1.x, w1.y), sm4(w1.z, w1.w));
-      }
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
+    // the bulk stores are the only step that needs the prefix
     if (tid == 0) {
       int ka = 0;
       while (ka < x.nblk) {
