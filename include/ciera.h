@@ -174,7 +174,7 @@ int ciera_status(void *workspace_dev, void *stream);
  * no device allocator of their own).  The paper has no counterpart: this is
  * ciera_compress with the same arguments and results, except that its
  * scratch (ticket counter, status word, look-back words, flag bytes) lives
- * in a fixed 4 MiB device array inside the library, which every GPU that
+ * in a fixed 8 MiB device array inside the library, which every GPU that
  * loads the library holds until the process exits.
  *   status_dev  optional (may be NULL): one device word the call sets to 0
  *               when its kernel finished normally, nonzero when a bounded
@@ -186,7 +186,7 @@ int ciera_status(void *workspace_dev, void *stream);
  * calls that can overlap on the GPU (other streams, other host threads)
  * race and must be serialised by the caller.
  * Errors: CIERA_E_INVAL as ciera_compress, and for a plan whose
- * info.workspace_bytes exceeds 4 MiB; CIERA_E_CUDA. */
+ * info.workspace_bytes exceeds 8 MiB; CIERA_E_CUDA. */
 int ciera_compress_noalloc(ciera_plan_t plan, int rank_begin, int rank_count,
                            const uint16_t *w_dev, uint8_t *sender_cache_dev, uint8_t *payloads_dev,
                            int64_t payload_stride, ciera_desc *descs_dev, uint8_t *flags_dev,

@@ -32,7 +32,7 @@ struct ciera_plan_s {
   int64_t capacity;
   int64_t flag_stride;
   int64_t nw_stride;
-  int64_t off_status, off_flags, off_words, off_prefix, off_rstate, ws_bytes;
+  int64_t off_status, off_tflags, off_flags, off_words, off_prefix, off_rstate, ws_bytes;
   int64_t smem_flags;       // dynamic shared memory of every compress call
   int64_t smem_compress;    // ... of a staged compress call
   int64_t smem_decompress;
@@ -136,7 +136,8 @@ int ciera_plan(const int64_t* shape, int ndim, int64_t block, int ranks, ciera_p
   p->flag_stride = align_up(p->nb_full > 0 ? p->nb_full : 1, 16);
   p->nw_stride = ceil_div(p->nb_full > 0 ? p->nb_full : 1, 32);
   p->off_status = 256;
-  p->off_flags = align_up(p->off_status + 8 * (p->total_tiles + 1), 256);
+  p->off_tflags = align_up(p->off_status + 8 * (p->total_tiles + 1), 256);
+  p->off_flags = align_up(p->off_tflags + 8 * (p->total_tiles + 1), 256);
   p->off_words = align_up(p->off_flags + p->flag_stride * ranks, 256);
   p->off_prefix = align_up(p->off_words + 4 * p->nw_stride * ranks, 256);
   p->off_rstate = align_up(p->off_prefix + 4 * p->nw_stride * ranks, 256);
@@ -204,6 +205,7 @@ int ciera_compress(ciera_plan_t p, int rank_begin, int rank_count, const uint16_
   kp.flagbytes = flags_dev ? flags_dev : ws + p->off_flags;
   kp.flag_stride = flags_dev ? p->nb_full : p->flag_stride;
   kp.tile_status = reinterpret_cast<unsigned long long*>(ws + p->off_status);
+  kp.tile_flags = reinterpret_cast<unsigned long long*>(ws + p->off_tflags);
   kp.ctl = reinterpret_cast<Control*>(ws);
   kp.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   kp.epoch = next_epoch();

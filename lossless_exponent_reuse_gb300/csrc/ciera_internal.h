@@ -29,7 +29,8 @@ struct Control {
 };
 enum : uint32_t { kStatusCorrupt = 1u, kStatusTimeout = 2u, kStatusInternal = 4u };
 
-// Decoupled look-back status word of one tile:
+// Decoupled look-back status word of one tile (and, beside it, an
+// epoch-tagged word with the tile's flag bits):
 //   bits 63..32 epoch of the call, bits 31..30 state, bits 29..0 count of
 //   changed blocks (aggregate of the tile, or inclusive prefix in its shard).
 enum : uint32_t { kStateAggregate = 1u, kStateInclusive = 2u };
@@ -63,6 +64,7 @@ struct CompressParams {
   uint8_t* flagbytes;           // per-rank rows of flag_stride bytes
   int64_t flag_stride;
   unsigned long long* tile_status;
+  unsigned long long* tile_flags;  // per tile: epoch << 32 | flag bits (tiles of <= 32 blocks)
   Control* ctl;
   uint64_t timeout_ns;
   uint32_t epoch;

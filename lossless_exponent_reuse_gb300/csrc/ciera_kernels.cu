@@ -52,6 +52,16 @@ __device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned l
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -251,11 +261,21 @@ __device__ __forceinline__ bool flag_of(const uint32_t* fw, int kb) {
 // ------------------------------------------------------------------------
 // Decoupled look-back over the per-tile count of changed blocks.
 
+// Tiles of at most 32 blocks also publish their flag bits in an
+// epoch-tagged word (tile_flags), which the shard's last tile polls for the
+// bitmap; their status words need no ordering and are stored relaxed.
+// Larger tiles (block size below 256) hand their flags over as flag bytes,
+// ordered by a release store of the status and read after an acquire.
+__device__ __forceinline__ bool flags_in_words(const CompressParams& p) { return p.geo.T <= 32; }
+
 __device__ __forceinline__ void publish(const CompressParams& p, const Tile& x, uint32_t state,
                                         uint32_t value) {
   const unsigned long long v = (static_cast<unsigned long long>(p.epoch) << 32) |
                                (static_cast<unsigned long long>(state) << 30) | value;
-  st_release_u64(&p.tile_status[x.sidx], v);
+  if (flags_in_words(p))
+    st_relaxed_u64(&p.tile_status[x.sidx], v);
+  else
+    st_release_u64(&p.tile_status[x.sidx], v);
 }
 
 // Warp-wide: the number of changed blocks in the tiles before x in its
@@ -284,7 +304,7 @@ __device__ uint32_t lookback_exclusive(const CompressParams& p, const Tile& x, u
     unsigned long long v = ep | incl;  // before the shard's first tile: inclusive 0
     if (idx >= gfirst) {
       for (;;) {
-        v = ld_acquire_u64(&st[idx]);
+        v = flags_in_words(p) ? ld_relaxed_u64(&st[idx]) : ld_acquire_u64(&st[idx]);
         if ((v >> 32) == p.epoch && ((v >> 30) & 3ull) != 0) break;
         const uint64_t now = globaltimer();
         if (!started) {
@@ -362,10 +382,12 @@ __device__ void publish_aggregate(const CompressParams& p, const Tile& x, const 
     flaggers_sync();
   }
   if (ft == 0) {
-    // the release of the status below orders these writes (and, through
-    // the fences above, those of the other flagging threads)
+    // with flag bytes, the release of the status below orders these writes
+    // (and, through the fences above, those of the other flagging threads)
     if (x.nblk <= 32)
       for (int kb = 0; kb < x.nblk; ++kb) fb[kb] = flag_of(fw, kb) ? 1 : 0;
+    if (flags_in_words(p))
+      st_relaxed_u64(&p.tile_flags[x.sidx], (static_cast<unsigned long long>(p.epoch) << 32) | fw[0]);
     uint32_t run = 0;
     for (int i = 0; i < nw; ++i) {
       fpre[i] = run;
@@ -400,7 +422,43 @@ __device__ void compress_epilogue(const CompressParams& p, const Tile& x, const 
     d.payload_bytes = static_cast<uint64_t>(raw ? 2 * x.len : body + bm);
     p.descs[x.rl] = d;
   }
-  if (!raw) {
+  if (raw) return;
+  if (flags_in_words(p)) {
+    // every tile of the shard stored its flag bits with this call's epoch;
+    // wait (bounded) until each word shows it
+    const unsigned long long* tf = p.tile_flags + (x.sidx - x.t);
+    const int64_t T = p.geo.T;
+    bool to = false;
+    for (int64_t i = tid; i < bm; i += blockDim.x) {
+      uint32_t byte = 0;
+      int64_t cur = -1;
+      uint32_t bits = 0;
+      for (int j = 0; j < 8; ++j) {
+        const int64_t k = 8 * i + j;
+        if (k >= x.nb) break;
+        const int64_t tj = k / T;
+        if (tj != cur) {
+          cur = tj;
+          unsigned long long v = ld_relaxed_u64(tf + tj);
+          if ((v >> 32) != p.epoch) {
+            const uint64_t t0 = globaltimer();
+            while ((v >> 32) != p.epoch) {
+              if (globaltimer() - t0 > p.timeout_ns) {
+                to = true;
+                break;
+              }
+              __nanosleep(32);
+              v = ld_relaxed_u64(tf + tj);
+            }
+          }
+          bits = static_cast<uint32_t>(v);
+        }
+        byte |= ((bits >> (k - tj * T)) & 1u) << j;
+      }
+      payload[body + i] = static_cast<uint8_t>(byte);
+    }
+    if (to) record_status(p.ctl, kStatusTimeout);
+  } else {
     // every earlier tile wrote its flag bytes before publishing its status;
     // read them from L2 (other CTAs wrote them during this launch)
     const uint8_t* fb = p.flagbytes + static_cast<int64_t>(x.rl) * p.flag_stride;
@@ -482,8 +540,9 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
       sh.X = X;
       if (to) record_status(p.ctl, kStatusTimeout);
     }
-    // the shard's last tile reads every other tile's flag bytes later on
-    if (x.t == x.tiles - 1) __threadfence();
+    // with flag bytes, the shard's last tile reads every other tile's flag
+    // bytes later on
+    if (x.t == x.tiles - 1 && !flags_in_words(p)) __threadfence();
     if (stg) mbar_wait_bounded(&bar, 0, p.timeout_ns);  // this warp reads ws/cs too
   } else {
     const int ft = tid - 32;

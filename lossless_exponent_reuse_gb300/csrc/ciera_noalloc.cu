@@ -20,10 +20,10 @@
 
 namespace {
 
-// Fixed scratch, shared by every call on a device.  4 MiB covers plans whose
+// Fixed scratch, shared by every call on a device.  8 MiB covers plans whose
 // workspace (ciera_plan_info_t.workspace_bytes) is at most this size, e.g.
 // 2.4e9 values over 32 ranks in blocks of 4096.
-constexpr size_t kScratchBytes = size_t(4) << 20;
+constexpr size_t kScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;

@@ -65,8 +65,8 @@ def test_noalloc_compress_matches_workspace_compress_two_calls():
 
 
 def test_noalloc_rejects_plans_larger_than_its_scratch():
-    plan = ciera.Plan(1 << 31, 256, 64)       # workspace far beyond 4 MiB
-    assert plan.info.workspace_bytes > (4 << 20)
+    plan = ciera.Plan(1 << 31, 256, 64)       # workspace far beyond 8 MiB
+    assert plan.info.workspace_bytes > (8 << 20)
     fake = ctypes.c_void_p(4096)              # never dereferenced: the size check fails first
     L = ciera.lib()
     assert L.ciera_compress_noalloc(plan.handle, 0, 64, fake, fake, fake,
