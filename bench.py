@@ -149,6 +149,22 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------
 
+def traffic_per_value(kernel):
+    """DRAM bytes per value of `kernel` from profiles/traffic.md, or None if
+    that capture was taken on a different kernel source."""
+    import hashlib
+    src = os.path.join(ROOT, "lossless_exponent_reuse_gb300", "csrc", "ciera_kernels.cu")
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for line in open(os.path.join(ROOT, "profiles", "traffic.md")):
+            cells = [c.strip() for c in line.strip().strip("|").split("|")]
+            if len(cells) >= 3 and cells[0] == kernel and cells[1] == h:
+                return float(cells[2])
+    except (OSError, ValueError):
+        pass
+    return None
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -354,6 +370,8 @@ def run_ours(args, world, rank, local):
     else:
         dom, dom_bytes, dom_ms = "k_bitmap_scan+k_decompress", statistics.mean(bytes_d) / L, md / L
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    tpv = traffic_per_value("k_compress" if dom == "k_compress" else "k_decompress")
+    traffic = round(tpv * n) if tpv is not None else None
     cfg = {"workload": wl.name, "numel": n * L, "layers": L, "numel_per_plan": n,
            "ranks": wl.ranks, "block": wl.block, "step": wl.steps[0],
            "iterations_timed": f"{W}..{W + K - 1}", "parallelism": f"replicas{world}",
@@ -371,7 +389,7 @@ def run_ours(args, world, rank, local):
         "kernels_ms": {"compress": round(mc, 4), "decompress": round(md, 4)},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": None, "peak_kind": peak_kind},
+                     "traffic": traffic, "peak_kind": peak_kind},
         "gpu_launches": K * L * 3,
         "clocks": clk,
     }
