@@ -197,6 +197,24 @@ int ciera_compress_noalloc(ciera_plan_t plan, int rank_begin, int rank_count,
  * compress iff (2N - P)/link_Bps > t_fixed_s + (4 + q)*N/hbm_Bps. */
 int ciera_should_compress(int64_t numel);
 
+/* Benefit-driven shard selection (Section 3.2): which of n shards to
+ * compress when the receivers' exponent caches may use at most
+ * cache_budget_bytes per GPU.  Shard i holds numel[i] bf16 values and has
+ * block change rate q[i] in [0, 1] (measured offline).  With the process-wide
+ * cost model:
+ *   gain      g_i = (2 N_i - (N_i + ceil(ceil(N_i/B)/8) + q_i N_i)) / link_Bps
+ *                   - (t_fixed_s + (4 + q_i) N_i / hbm_Bps)
+ *   footprint M_i = (world - 1) N_i bytes (exponents of the other ranks' shards)
+ * Shards with g_i > 0 are taken in descending order of g_i / M_i (equal
+ * ratios: lower index first) while the total footprint fits the budget; a
+ * shard that does not fit is skipped and later, smaller ones may still fit.
+ * Outputs (host arrays of n): selected[i] = 1 if selected, gain[i] = g_i in
+ * seconds per iteration.  The selection is made once and kept for the run.
+ * Returns the number selected, or CIERA_E_INVAL (n < 0, world < 1, negative
+ * budget or size, q outside [0, 1], NULL arrays with n > 0). */
+int ciera_bsc_select(const int64_t *numel, const double *q, int n, int world,
+                     int64_t cache_budget_bytes, uint8_t *selected, double *gain);
+
 /* Replace / read the process-wide cost model.  Defaults: link 8e9 B/s,
  * q_hat 0.22, t_fixed 20e-6 s, hbm 8e12 B/s, block 4096.
  * Errors: CIERA_E_INVAL for NULL, non-positive rates, q_hat outside [0,1],

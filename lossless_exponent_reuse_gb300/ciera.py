@@ -70,6 +70,7 @@ SIGNATURES = {
                                       _vp]),
     "ciera_status": (_i32, [_vp, _vp]),
     "ciera_should_compress": (_i32, [_i64]),
+    "ciera_bsc_select": (_i32, [_vp, _vp, _i32, _i32, _i64, _vp, _vp]),
     "ciera_set_cost_model": (_i32, [ctypes.POINTER(_CostModel)]),
     "ciera_get_cost_model": (_i32, [ctypes.POINTER(_CostModel)]),
     "ciera_set_wait_timeout_ns": (_i32, [ctypes.c_uint64]),
@@ -245,6 +246,22 @@ def status(workspace: torch.Tensor, stream=None) -> int:
 
 def should_compress(numel: int) -> bool:
     return bool(lib().ciera_should_compress(int(numel)))
+
+
+def bsc_select(numel, q, world: int, cache_budget_bytes: int):
+    """ciera_bsc_select: returns (selected: list[bool], gain: list[float])."""
+    import numpy as np
+    numel = np.ascontiguousarray(numel, dtype=np.int64)
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    n = numel.size
+    sel = np.zeros(max(n, 1), dtype=np.uint8)
+    gain = np.zeros(max(n, 1), dtype=np.float64)
+    st = lib().ciera_bsc_select(numel.ctypes.data if n else None, q.ctypes.data if n else None,
+                                n, int(world), int(cache_budget_bytes), sel.ctypes.data,
+                                gain.ctypes.data)
+    if st < 0:
+        raise CieraError(st, "ciera_bsc_select")
+    return [bool(x) for x in sel[:n]], [float(x) for x in gain[:n]]
 
 
 def set_cost_model(link_Bps=8e9, q_hat=0.22, t_fixed_s=20e-6, hbm_Bps=8e12, block=4096) -> None:

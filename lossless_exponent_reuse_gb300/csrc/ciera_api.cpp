@@ -6,11 +6,13 @@
 // Section 3.2 (block count, bitmap size, gain of a shard).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "ciera.h"
 #include "ciera_internal.h"
@@ -281,6 +283,49 @@ int ciera_should_compress(int64_t numel) {
   const double saved_s = (2.0 * n - payload) / m.link_Bps;
   const double decompress_s = m.t_fixed_s + (4.0 + m.q_hat) * n / m.hbm_Bps;
   return saved_s > decompress_s ? 1 : 0;
+}
+
+int ciera_bsc_select(const int64_t* numel, const double* q, int n, int world,
+                     int64_t cache_budget_bytes, uint8_t* selected, double* gain) {
+  if (n < 0 || world < 1 || cache_budget_bytes < 0 ||
+      (n > 0 && (!numel || !q || !selected || !gain)))
+    return CIERA_E_INVAL;
+  for (int i = 0; i < n; ++i)
+    if (numel[i] < 0 || !(q[i] >= 0.0) || !(q[i] <= 1.0)) return CIERA_E_INVAL;
+  ciera_cost_model m;
+  {
+    std::lock_guard<std::mutex> lk(g_cost_mu);
+    m = g_cost;
+  }
+  // Section 3.2: g_i = Comm(S_i) - Comm(S_s+m + S_bm + q_i S_e) - T_decmp,
+  // with the exponents of the other W-1 ranks' shards as cache footprint.
+  std::vector<int> cand;
+  std::vector<double> ratio(static_cast<size_t>(n > 0 ? n : 0));
+  for (int i = 0; i < n; ++i) {
+    const double v = static_cast<double>(numel[i]);
+    const double bitmap = static_cast<double>(ceil_div(ceil_div(numel[i], m.block), 8));
+    const double saved_s = (2.0 * v - (v + bitmap + q[i] * v)) / m.link_Bps;
+    const double decompress_s = m.t_fixed_s + (4.0 + q[i]) * v / m.hbm_Bps;
+    gain[i] = saved_s - decompress_s;
+    selected[i] = 0;
+    const double footprint = static_cast<double>(world - 1) * v;
+    ratio[i] = footprint > 0 ? gain[i] / footprint : 0.0;
+    if (gain[i] > 0 && footprint > 0) cand.push_back(i);
+  }
+  // best benefit per cached byte first; equal ratios keep their order
+  std::stable_sort(cand.begin(), cand.end(),
+                   [&](int a, int b) { return ratio[a] > ratio[b]; });
+  int taken = 0;
+  int64_t used = 0;
+  for (int i : cand) {
+    const int64_t footprint = static_cast<int64_t>(world - 1) * numel[i];
+    if (footprint <= cache_budget_bytes - used) {
+      used += footprint;
+      selected[i] = 1;
+      ++taken;
+    }
+  }
+  return taken;
 }
 
 int ciera_set_cost_model(const ciera_cost_model* model) {

@@ -88,6 +88,10 @@ def lib() -> ctypes.CDLL:
             L.oracle_should_compress.argtypes = [i64, ctypes.c_double, ctypes.c_double,
                                                  ctypes.c_double, ctypes.c_double, i64]
             L.oracle_should_compress.restype = ctypes.c_int
+            L.oracle_bsc_select.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, i64,
+                                            ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                            i64, vp, vp]
+            L.oracle_bsc_select.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -215,3 +219,17 @@ DEFAULT_COST_MODEL = dict(link_Bps=8e9, q_hat=0.22, t_fixed_s=20e-6, hbm_Bps=8e1
 def should_compress(numel: int, link_Bps=8e9, q_hat=0.22, t_fixed_s=20e-6, hbm_Bps=8e12,
                     block=4096) -> bool:
     return bool(lib().oracle_should_compress(numel, link_Bps, q_hat, t_fixed_s, hbm_Bps, block))
+
+
+def bsc_select(numel, q, world: int, budget_bytes: int, link_Bps=8e9, t_fixed_s=20e-6,
+               hbm_Bps=8e12, block=4096):
+    """Section 3.2 shard selection.  Returns (selected u8[n], gain f64[n], count)."""
+    numel = np.ascontiguousarray(numel, dtype=np.int64)
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    n = numel.size
+    sel = np.zeros(max(n, 1), dtype=np.uint8)
+    gain = np.zeros(max(n, 1), dtype=np.float64)
+    cnt = lib().oracle_bsc_select(_ptr(numel) if n else None, _ptr(q) if n else None, n, world,
+                                  budget_bytes, link_Bps, t_fixed_s, hbm_Bps, block, _ptr(sel),
+                                  _ptr(gain))
+    return sel[:n], gain[:n], int(cnt)

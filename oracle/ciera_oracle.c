@@ -49,6 +49,7 @@
 #include <stddef.h>
 #include <string.h>
 #include <math.h>
+#include <stdlib.h>
 
 /* Descriptor of one rank's payload.  Field order and widths are part of the
  * payload format: mode (0 compressed, 1 raw), number of changed blocks,
@@ -346,4 +347,79 @@ int oracle_should_compress(int64_t numel, double link_Bps, double q_hat,
     double saved = (2.0 * n - payload) / link_Bps;
     double cost = t_fixed_s + (4.0 + q_hat) * n / hbm_Bps;
     return saved > cost ? 1 : 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Section 3.2: benefit-driven selective compression (BSC).
+ *
+ * Shard i holds N_i bf16 values: S_i = 2 N_i bytes, S_e,i = N_i exponent
+ * bytes, S_s+m,i = N_i sign+mantissa bytes; its bitmap has
+ * ceil(ceil(N_i/B)/8) bytes and q_i is its block change rate.
+ *   gain      g_i = (S_i - (S_s+m,i + S_bm,i + q_i S_e,i)) / link
+ *                   - (t_fixed + (4 + q_i) N_i / hbm)          (reading R6)
+ *   footprint M_i = (W - 1) S_e,i   (exponents cached for the other ranks)
+ * Shards with g_i > 0 are taken in descending order of g_i / M_i (ties: lower
+ * index first) while the running footprint stays within the budget; a shard
+ * that does not fit is skipped and smaller ones after it may still fit.
+ * Returns the number selected; selected[i] = 1 for a selected shard.
+ */
+static double oracle_bsc_gain(int64_t n, double q, double link_Bps, double t_fixed_s,
+                              double hbm_Bps, int64_t block)
+{
+    double nn = (double)n;
+    double nblocks = (double)((n + block - 1) / block);
+    double bitmap = ceil(nblocks / 8.0);
+    double full = 2.0 * nn;
+    double payload = nn + bitmap + q * nn;
+    double saved = (full - payload) / link_Bps;
+    double decompress = t_fixed_s + (4.0 + q) * nn / hbm_Bps;
+    return saved - decompress;
+}
+
+int oracle_bsc_select(const int64_t *numel, const double *q, int n, int world,
+                      int64_t budget_bytes, double link_Bps, double t_fixed_s,
+                      double hbm_Bps, int64_t block, uint8_t *selected, double *gain)
+{
+    int i, j, taken = 0;
+    int64_t used = 0;
+    /* candidates: positive gain; order by ratio, descending, stable */
+    int order_len = 0;
+    int *order = (int *)malloc(sizeof(int) * (size_t)(n > 0 ? n : 1));
+    double *ratio = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    if (!order || !ratio) {
+        free(order);
+        free(ratio);
+        return -1;
+    }
+    for (i = 0; i < n; ++i) {
+        double footprint = (double)(world - 1) * (double)numel[i];
+        gain[i] = oracle_bsc_gain(numel[i], q[i], link_Bps, t_fixed_s, hbm_Bps, block);
+        selected[i] = 0;
+        ratio[i] = footprint > 0 ? gain[i] / footprint : 0.0;
+        if (gain[i] > 0 && footprint > 0) {
+            order[order_len++] = i;
+        }
+    }
+    /* insertion sort: descending ratio, ties keep index order */
+    for (i = 1; i < order_len; ++i) {
+        int cur = order[i];
+        j = i - 1;
+        while (j >= 0 && ratio[order[j]] < ratio[cur]) {
+            order[j + 1] = order[j];
+            --j;
+        }
+        order[j + 1] = cur;
+    }
+    for (i = 0; i < order_len; ++i) {
+        int s = order[i];
+        int64_t footprint = (int64_t)(world - 1) * numel[s];
+        if (used + footprint <= budget_bytes) {
+            used += footprint;
+            selected[s] = 1;
+            ++taken;
+        }
+    }
+    free(order);
+    free(ratio);
+    return taken;
 }
