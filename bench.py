@@ -52,6 +52,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--variant", default="")
+    ap.add_argument("--sender", choices=["exact", "hash"], default="exact",
+                    help="change test: exact exponent compare (default) or the 128-bit "
+                         "block hash with a 16-byte-per-block HashCache")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -174,7 +177,7 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def algorithmic_bytes(descs, numel):
+def algorithmic_bytes(descs, numel, hashed=False, block=4096):
     """(compress bytes, decompress bytes, changed fraction) of one step.
 
     compress:   read w 2N + sender cache N, write payloads P + exponents of
@@ -189,6 +192,14 @@ def algorithmic_bytes(descs, numel):
     comp_vals = numel - raw_vals
     comp_changed = sum(d["body_bytes"] for d in descs if d["mode"] == 0) - comp_vals
     C = raw_vals + comp_changed
+    if hashed:
+        # hashed sender: reads w 2N + 16 B of HashCache per block, writes
+        # payloads P + 16 B per changed block
+        R = len(descs)
+        S = -(-numel // R)
+        blocks = sum(-(-max(0, min(S, numel - r * S)) // block) for r in range(R))
+        changed = sum(d["n_changed_blocks"] for d in descs)
+        return 2 * numel + 16 * blocks + P + 16 * changed, 3 * numel + P, C / max(numel, 1)
     return 3 * numel + P + C, 3 * numel + P, C / max(numel, 1)
 
 
@@ -283,7 +294,9 @@ def run_ours(args, world, rank, local):
     n = sum(k for _, k in acc)                      # values per layer on the path
     L = wl.layers
     gen = iteration_buckets(wl, W + K, dev)
-    layers = [SimulatedAllgather(n, wl.block, wl.ranks, device=dev) for _ in range(L)]
+    hashed = args.sender == "hash"
+    layers = [SimulatedAllgather(n, wl.block, wl.ranks, device=dev, hashed=hashed)
+              for _ in range(L)]
     stream = torch.cuda.current_stream()
     warm_host = []                                  # iterations W-1, W of layer 0 for the oracle
     for t in range(W):
@@ -298,7 +311,8 @@ def run_ours(args, world, rank, local):
     seq = [next(gen) for _ in range(K)]             # timed inputs, resident in HBM
     warm_host.append(seq[0][0].view(torch.int16).cpu().numpy().view(np.uint16))
     del gen
-    snaps = [(ag.sender_cache.clone(), ag.recv_cache.clone()) for ag in layers]
+    snaps = [(ag.hash_cache.clone() if hashed else ag.sender_cache.clone(), ag.recv_cache.clone())
+             for ag in layers]
     it0 = layers[0].iteration
     torch.cuda.synchronize()
 
@@ -328,13 +342,14 @@ def run_ours(args, world, rank, local):
     total_ms = start.elapsed_time(end)
     t_c = [sum(ev[i][li][0].elapsed_time(ev[i][li][1]) for li in range(L)) for i in range(K)]
     t_d = [sum(ev[i][li][1].elapsed_time(ev[i][li][2]) for li in range(L)) for i in range(K)]
-    finals = [(ag.out.view(torch.int16).clone(), ag.sender_cache.clone(), ag.recv_cache.clone())
-              for ag in layers]
+    finals = [(ag.out.view(torch.int16).clone(),
+               ag.hash_cache.clone() if hashed else ag.sender_cache.clone(),
+               ag.recv_cache.clone()) for ag in layers]
 
     # untimed replay from the same state: per-step descriptors for the byte
     # accounting, and a determinism check against the timed run
     for ag, (sc, rc) in zip(layers, snaps):
-        ag.sender_cache.copy_(sc)
+        (ag.hash_cache if hashed else ag.sender_cache).copy_(sc)
         ag.recv_cache.copy_(rc)
         ag.iteration = it0
     del snaps
@@ -343,7 +358,7 @@ def run_ours(args, world, rank, local):
         bc = bd = fsum = 0.0
         for li, ag in enumerate(layers):
             ag.compress(seq[i][li])
-            c_, d_, f_ = algorithmic_bytes(ag.descriptors(), n)
+            c_, d_, f_ = algorithmic_bytes(ag.descriptors(), n, hashed, wl.block)
             bc, bd, fsum = bc + c_, bd + d_, fsum + f_
             ag.decompress()
         bytes_c.append(bc)
@@ -351,7 +366,8 @@ def run_ours(args, world, rank, local):
         fvals.append(fsum / L)
     torch.cuda.synchronize()
     for ag, (o, sc, rc) in zip(layers, finals):
-        if not (torch.equal(o, ag.out.view(torch.int16)) and torch.equal(sc, ag.sender_cache)
+        if not (torch.equal(o, ag.out.view(torch.int16))
+                and torch.equal(sc, ag.hash_cache if hashed else ag.sender_cache)
                 and torch.equal(rc, ag.recv_cache)):
             raise RuntimeError("replay differs from the timed run")
     for ag, w in zip(layers, seq[-1]):
@@ -370,9 +386,11 @@ def run_ours(args, world, rank, local):
     else:
         dom, dom_bytes, dom_ms = "k_bitmap_scan+k_decompress", statistics.mean(bytes_d) / L, md / L
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-    tpv = traffic_per_value("k_compress" if dom == "k_compress" else "k_decompress")
+    tpv = traffic_per_value(("k_compress_hashed" if hashed else "k_compress")
+                            if dom == "k_compress" else "k_decompress")
     traffic = round(tpv * n) if tpv is not None else None
-    cfg = {"workload": wl.name, "numel": n * L, "layers": L, "numel_per_plan": n,
+    cfg = {"workload": wl.name, "sender": args.sender, "numel": n * L, "layers": L,
+           "numel_per_plan": n,
            "ranks": wl.ranks, "block": wl.block, "step": wl.steps[0],
            "iterations_timed": f"{W}..{W + K - 1}", "parallelism": f"replicas{world}",
            "l2": f"inputs larger than L2 ({2 * n / 1e6:.0f} MB of weights per plan), no flush"}
@@ -398,7 +416,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.empty_cache()
     if not args.no_e2e:
         if L == 1:
-            result["e2e"] = run_e2e(wl, [s_[0] for s_ in seq], n, K, dev, world)
+            result["e2e"] = run_e2e(wl, [s_[0] for s_ in seq], n, K, dev, world, hashed)
         else:
             result["e2e"] = None
     del seq
@@ -407,7 +425,7 @@ def run_ours(args, world, rank, local):
     return result
 
 
-def run_e2e(wl, seq, n, K, dev, world):
+def run_e2e(wl, seq, n, K, dev, world, hashed=False):
     """The same metric through host buffers: each step copies its weights
     from pinned host memory, runs the path and reads the result back.
     A fresh state is warmed up on the first three inputs (the first call is
@@ -417,7 +435,7 @@ def run_e2e(wl, seq, n, K, dev, world):
     host = [s.view(torch.int16).to("cpu").pin_memory() for s in seq]
     out_host = torch.empty(n, dtype=torch.int16).pin_memory()
     w_dev = torch.empty(n, dtype=torch.int16, device=dev)
-    ag = SimulatedAllgather(n, wl.block, wl.ranks, device=dev)
+    ag = SimulatedAllgather(n, wl.block, wl.ranks, device=dev, hashed=hashed)
     stream = torch.cuda.current_stream()
     for t in range(min(3, len(host))):               # warm-up (first call is the cold start)
         ag.step_host(host[t], out_host, w_dev)

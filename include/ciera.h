@@ -150,6 +150,28 @@ int ciera_compress(ciera_plan_t plan, int rank_begin, int rank_count, const uint
                    ciera_desc *descs_dev, uint8_t *flags_dev, void *workspace_dev, uint32_t flags,
                    void *stream);
 
+/* Sender side with the paper's change test (Section 3.1; Algorithm 1,
+ * "Hash128" and "HashCache"): block k is changed iff the 128-bit hash of its
+ * exponents differs from hash_cache's entry for k (always on a cold start),
+ * and a changed block's entry is replaced.  Same payloads, descriptors and
+ * flags as ciera_compress whenever no two exponent sequences of a block
+ * collide in 128 bits; the sender keeps 16 bytes per block instead of one
+ * exponent byte per value, and reads 2 instead of 3 bytes per value.
+ * Hash of a block of L exponents e_0..e_{L-1}, per seed s:
+ *   h_s = fin(L + sum_j fin(word_j XOR splitmix64(s, j + 1)))   (mod 2^64)
+ * with word_j = e_{8j} | e_{8j+1} << 8 | ... | e_{8j+7} << 56 (missing
+ * exponents 0), splitmix64(s, i) the i-th output of SplitMix64 started at
+ * state s, fin its output function, and seeds s1 = 0x6a09e667f3bcc908,
+ * s2 = 0xbb67ae8584caa73b.
+ *   hash_cache_dev  rank_count rows of blocks_per_shard entries of two
+ *                   uint64 (h_s1, h_s2); updated in place
+ * Other arguments as ciera_compress.  Errors: as ciera_compress, and
+ * CIERA_E_INVAL when a tile holds more than 32 blocks (block < 256). */
+int ciera_compress_hashed(ciera_plan_t plan, int rank_begin, int rank_count,
+                          const uint16_t *w_dev, uint64_t *hash_cache_dev, uint8_t *payloads_dev,
+                          int64_t payload_stride, ciera_desc *descs_dev, uint8_t *flags_dev,
+                          void *workspace_dev, uint32_t flags, void *stream);
+
 /* Receiver side (Section 3.1; Algorithm 1, receiver): rebuilds all N values
  * from the R payloads and refreshes the receiver's exponent cache.
  *   payloads_dev   R payloads, rank r's at payloads_dev + r*payload_stride

@@ -22,12 +22,17 @@ class SimulatedAllgather:
     """Device state of one plan: both exponent caches, payloads, descriptors."""
 
     def __init__(self, numel: int, block: int, ranks: int, device="cuda",
-                 keep_flags: bool = False):
+                 keep_flags: bool = False, hashed: bool = False):
         self.plan = ciera.Plan(numel, block, ranks)
         info = self.plan.info
         self.numel = numel
         self.device = torch.device(device)
-        self.sender_cache = torch.zeros(max(numel, 1), dtype=torch.uint8, device=device)
+        self.hashed = hashed
+        # the sender's state: exponents per value, or (hashed) 16 bytes per block
+        self.hash_cache = (torch.zeros((ranks, max(info.blocks_per_shard, 1), 2),
+                                       dtype=torch.int64, device=device) if hashed else None)
+        self.sender_cache = torch.zeros(1 if hashed else max(numel, 1), dtype=torch.uint8,
+                                        device=device)
         self.recv_cache = torch.zeros(max(numel, 1), dtype=torch.uint8, device=device)
         self.payloads = self.plan.new_payloads(device=device)
         self.descs = self.plan.new_descs(device=device)
@@ -38,8 +43,13 @@ class SimulatedAllgather:
         self.iteration = 0
 
     def compress(self, w: torch.Tensor, stream=None) -> None:
-        self.plan.compress(w, self.sender_cache, self.payloads, self.descs, self.workspace,
-                           cold=self.iteration == 0, flags_out=self.flags, stream=stream)
+        if self.hashed:
+            self.plan.compress_hashed(w, self.hash_cache, self.payloads, self.descs,
+                                      self.workspace, cold=self.iteration == 0,
+                                      flags_out=self.flags, stream=stream)
+        else:
+            self.plan.compress(w, self.sender_cache, self.payloads, self.descs, self.workspace,
+                               cold=self.iteration == 0, flags_out=self.flags, stream=stream)
 
     def decompress(self, stream=None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
         o = self.out if out is None else out

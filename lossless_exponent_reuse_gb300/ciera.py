@@ -66,6 +66,8 @@ SIGNATURES = {
     "ciera_workspace_init": (_i32, [_vp, _vp, _vp]),
     "ciera_compress": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _u32, _vp]),
     "ciera_decompress": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _u32, _vp]),
+    "ciera_compress_hashed": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _u32,
+                                     _vp]),
     "ciera_compress_noalloc": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _u32,
                                       _vp]),
     "ciera_status": (_i32, [_vp, _vp]),
@@ -215,6 +217,30 @@ class Plan:
             _dev_ptr(descs, "descs", torch.uint8), _dev_ptr(flags_out, "flags_out", torch.uint8),
             _dev_ptr(workspace, "workspace", torch.uint8), flags, _stream_handle(stream)),
             "ciera_compress")
+
+    def compress_hashed(self, w: torch.Tensor, hash_cache: torch.Tensor, payloads: torch.Tensor,
+                        descs: torch.Tensor, workspace: torch.Tensor, *, cold: bool = False,
+                        rank_begin: int = 0, rank_count: Optional[int] = None,
+                        flags_out: Optional[torch.Tensor] = None, stream=None) -> None:
+        """ciera_compress_hashed: ``hash_cache`` holds 16 bytes per block
+        (rank_count x blocks_per_shard x 2 uint64, any 8-byte dtype)."""
+        info = self.info
+        rc = info.ranks - rank_begin if rank_count is None else rank_count
+        if payloads.dim() != 2 or payloads.shape[0] < rc:
+            raise ValueError("payloads must be [rank_count, stride] uint8")
+        if descs.numel() < rc * DESC_BYTES:
+            raise ValueError("descs too small")
+        if hash_cache.numel() * hash_cache.element_size() < 16 * rc * info.blocks_per_shard:
+            raise ValueError("hash_cache too small")
+        if workspace.numel() < info.workspace_bytes:
+            raise ValueError("workspace too small")
+        _check(lib().ciera_compress_hashed(
+            self._h, int(rank_begin), int(rc), _dev_ptr(w, "w", torch.uint16),
+            _dev_ptr(hash_cache, "hash_cache"),
+            _dev_ptr(payloads, "payloads", torch.uint8), payloads.stride(0),
+            _dev_ptr(descs, "descs", torch.uint8), _dev_ptr(flags_out, "flags_out", torch.uint8),
+            _dev_ptr(workspace, "workspace", torch.uint8), COLD if cold else 0,
+            _stream_handle(stream)), "ciera_compress_hashed")
 
     def decompress(self, payloads: torch.Tensor, descs: torch.Tensor, recv_cache: torch.Tensor,
                    out: torch.Tensor, workspace: torch.Tensor, *, stream=None) -> None:

@@ -35,8 +35,8 @@ struct ciera_plan_s {
   int64_t flag_stride;
   int64_t nw_stride;
   int64_t off_status, off_tflags, off_flags, off_words, off_prefix, off_rstate, ws_bytes;
-  int64_t smem_flags;       // dynamic shared memory of every compress call
-  int64_t smem_compress;    // ... of a staged compress call
+  int64_t smem_flags;         // flag words of every compress call (exact test)
+  int64_t smem_flags_hashed;  // ... plus the per-block hash sums (hashed test)
   int64_t smem_decompress;
   bool fast;
   bool raw_fixup;
@@ -44,21 +44,12 @@ struct ciera_plan_s {
 
 namespace {
 
-std::atomic<uint32_t> g_epoch{0};
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 std::mutex g_cost_mu;
 ciera_cost_model g_cost = {8e9, 0.22, 20e-6, 8e12, 4096};
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t align_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
-
-uint32_t next_epoch() {
-  uint32_t e;
-  do {
-    e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
-  } while (e == 0);  // a zero-filled workspace holds epoch 0: never valid
-  return e;
-}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -149,7 +140,7 @@ int ciera_plan(const int64_t* shape, int ndim, int64_t block, int ranks, ciera_p
   // compress: flag words + their prefix (every call), then 2*TE values and
   // TE exponents (staged calls only)
   p->smem_flags = align_up(8 * ceil_div(p->T, 32), 128);
-  p->smem_compress = p->smem_flags + (p->fast ? 3 * p->T * block : 0);
+  p->smem_flags_hashed = align_up(align_up(8 * ceil_div(p->T, 32), 16) + 32 * p->T, 128);
   p->smem_decompress = p->fast ? 4 * p->T * block : 0;
   p->raw_fixup = raw_can_hold_unchanged(p->S, block) ||
                  raw_can_hold_unchanged(p->len_part, block);
@@ -182,17 +173,25 @@ int ciera_workspace_init(ciera_plan_t p, void* workspace_dev, void* stream) {
   return e == cudaSuccess ? CIERA_OK : CIERA_E_CUDA;
 }
 
-int ciera_compress(ciera_plan_t p, int rank_begin, int rank_count, const uint16_t* w_dev,
-                   uint8_t* sender_cache_dev, uint8_t* payloads_dev, int64_t payload_stride,
-                   ciera_desc* descs_dev, uint8_t* flags_dev, void* workspace_dev, uint32_t flags,
-                   void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of ciera_compress and ciera_compress_hashed.  Exactly one of
+// sender_cache_dev / hash_cache_dev is used.
+int compress_impl(ciera_plan_t p, int rank_begin, int rank_count, const uint16_t* w_dev,
+                  uint8_t* sender_cache_dev, uint64_t* hash_cache_dev, bool hashed,
+                  uint8_t* payloads_dev, int64_t payload_stride, ciera_desc* descs_dev,
+                  uint8_t* flags_dev, void* workspace_dev, uint32_t flags, void* stream) {
   if (!p || rank_begin < 0 || rank_count < 1 ||
       static_cast<int64_t>(rank_begin) + rank_count > p->ranks)
     return CIERA_E_INVAL;
   if (!payloads_dev || !descs_dev || !workspace_dev || payload_stride < p->capacity)
     return CIERA_E_INVAL;
+  if (hashed && p->T > 32) return CIERA_E_INVAL;  // block below 256 values
   const Geometry g = range_geometry(p, rank_begin, rank_count);
-  if (g.total_tiles > 0 && (!w_dev || !sender_cache_dev)) return CIERA_E_INVAL;
+  if (g.total_tiles > 0 && (!w_dev || (hashed ? !hash_cache_dev : !sender_cache_dev)))
+    return CIERA_E_INVAL;
   const uint32_t known = CIERA_COLD | CIERA_DEBUG_SKIP_FIRST_PUBLISH;
   if (flags & ~known) return CIERA_E_INVAL;
 
@@ -201,6 +200,9 @@ int ciera_compress(ciera_plan_t p, int rank_begin, int rank_count, const uint16_
   kp.geo = g;
   kp.w = w_dev;
   kp.scache = sender_cache_dev;
+  kp.hash_cache = reinterpret_cast<unsigned long long*>(hash_cache_dev);
+  kp.hash_stride = p->nb_full;
+  kp.hashed = hashed ? 1 : 0;
   kp.payloads = payloads_dev;
   kp.stride = payload_stride;
   kp.descs = descs_dev;
@@ -210,13 +212,36 @@ int ciera_compress(ciera_plan_t p, int rank_begin, int rank_count, const uint16_
   kp.tile_flags = reinterpret_cast<unsigned long long*>(ws + p->off_tflags);
   kp.ctl = reinterpret_cast<Control*>(ws);
   kp.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
-  kp.epoch = next_epoch();
   kp.flags = flags;
-  kp.fast = p->fast && aligned16(w_dev) && aligned16(sender_cache_dev) &&
-            aligned16(payloads_dev) && (payload_stride % 16 == 0);
-  const int e = launch_compress(kp, kp.fast ? p->smem_compress : p->smem_flags,
-                               p->raw_fixup ? 1 : 0, stream);
+  kp.fast = p->fast && aligned16(w_dev) && aligned16(payloads_dev) &&
+            (payload_stride % 16 == 0) &&
+            (hashed ? aligned16(hash_cache_dev) : aligned16(sender_cache_dev));
+  const int64_t flag_region = hashed ? p->smem_flags_hashed : p->smem_flags;
+  const int64_t smem = flag_region + (kp.fast ? 3 * p->T * p->block : 0);
+  const int e = launch_compress(kp, smem, p->raw_fixup ? 1 : 0, stream);
   return e == cudaSuccess ? CIERA_OK : CIERA_E_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ciera_compress(ciera_plan_t p, int rank_begin, int rank_count, const uint16_t* w_dev,
+                   uint8_t* sender_cache_dev, uint8_t* payloads_dev, int64_t payload_stride,
+                   ciera_desc* descs_dev, uint8_t* flags_dev, void* workspace_dev, uint32_t flags,
+                   void* stream) {
+  return compress_impl(p, rank_begin, rank_count, w_dev, sender_cache_dev, nullptr, false,
+                       payloads_dev, payload_stride, descs_dev, flags_dev, workspace_dev, flags,
+                       stream);
+}
+
+int ciera_compress_hashed(ciera_plan_t p, int rank_begin, int rank_count, const uint16_t* w_dev,
+                          uint64_t* hash_cache_dev, uint8_t* payloads_dev, int64_t payload_stride,
+                          ciera_desc* descs_dev, uint8_t* flags_dev, void* workspace_dev,
+                          uint32_t flags, void* stream) {
+  return compress_impl(p, rank_begin, rank_count, w_dev, nullptr, hash_cache_dev, true,
+                       payloads_dev, payload_stride, descs_dev, flags_dev, workspace_dev, flags,
+                       stream);
 }
 
 int ciera_decompress(ciera_plan_t p, const uint8_t* payloads_dev, int64_t payload_stride,

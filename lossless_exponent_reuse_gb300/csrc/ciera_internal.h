@@ -23,15 +23,18 @@ constexpr int64_t kMaxShardBlocks = int64_t(1) << 30;  // fits the 30-bit prefix
 
 // Workspace control block at offset 0.
 struct Control {
-  uint32_t ticket;   // compress: next tile ticket; the last ticket resets it
+  // compress: (launch number << 32) | tickets drawn in the current launch;
+  // the last ticket resets the count and advances the launch number
+  unsigned long long ticket;
   uint32_t status;   // kStatus* bits, read and cleared by ciera_status
-  uint32_t pad[62];
+  uint32_t pad[61];
 };
 enum : uint32_t { kStatusCorrupt = 1u, kStatusTimeout = 2u, kStatusInternal = 4u };
 
 // Decoupled look-back status word of one tile (and, beside it, an
 // epoch-tagged word with the tile's flag bits):
-//   bits 63..32 epoch of the call, bits 31..30 state, bits 29..0 count of
+//   bits 63..32 the launch's tag (launch number + 1, never 0), bits 31..30
+//   state, bits 29..0 count of
 //   changed blocks (aggregate of the tile, or inclusive prefix in its shard).
 enum : uint32_t { kStateAggregate = 1u, kStateInclusive = 2u };
 
@@ -65,12 +68,14 @@ struct CompressParams {
   int64_t flag_stride;
   unsigned long long* tile_status;
   unsigned long long* tile_flags;  // per tile: epoch << 32 | flag bits (tiles of <= 32 blocks)
+  unsigned long long* hash_cache;  // hashed change test: 2 words per block
+  int64_t hash_stride;             // blocks per rank in hash_cache
   Control* ctl;
   uint64_t timeout_ns;
-  uint32_t epoch;
   uint32_t flags;
+  uint32_t pad2;
   int32_t fast;                 // staged path allowed for whole-16 tiles
-  int32_t pad;
+  int32_t hashed;               // 1: hashed change test (k_compress<true>)
 };
 
 struct DecompressParams {

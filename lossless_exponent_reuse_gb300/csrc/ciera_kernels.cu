@@ -152,6 +152,66 @@ __device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
 }
 
 // ------------------------------------------------------------------------
+// Hashed change test (Section 3.1, Hash128 / HashCache).  SplitMix64's
+// finalizer and increment (Steele, Lea and Flood, 2014); a block hash with
+// one seed is fin(L + sum_j fin(word_j ^ key_j)) where word_j packs exponents
+// 8j..8j+7 little-endian and key_j is SplitMix64's output j+1 from `seed`;
+// the sum is order-free, so threads add their words in any order.
+
+constexpr unsigned long long kGolden = 0x9e3779b97f4a7c15ull;
+constexpr unsigned long long kSeed1 = 0x6a09e667f3bcc908ull;
+constexpr unsigned long long kSeed2 = 0xbb67ae8584caa73bull;
+
+__device__ __forceinline__ unsigned long long sm64_fin(unsigned long long z) {
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  return z ^ (z >> 31);
+}
+
+// The keys (SplitMix64's outputs 1 .. kKeyWords from both seeds) of the
+// first kKeyWords exponent words of a block, evaluated at compile time.
+constexpr int kKeyWords = 2048;  // blocks of up to 16384 values
+
+constexpr unsigned long long sm64_fin_c(unsigned long long z) {
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  return z ^ (z >> 31);
+}
+
+struct HashKeys {
+  unsigned long long k[kKeyWords][2];
+};
+
+constexpr HashKeys make_hash_keys() {
+  HashKeys h{};
+  for (int j = 0; j < kKeyWords; ++j) {
+    const unsigned long long step = static_cast<unsigned long long>(j + 1) * kGolden;
+    h.k[j][0] = sm64_fin_c(kSeed1 + step);
+    h.k[j][1] = sm64_fin_c(kSeed2 + step);
+  }
+  return h;
+}
+
+__device__ const HashKeys g_hash_keys = make_hash_keys();
+
+// Both seeds' terms of exponent word number j (0-based) of a block.
+__device__ __forceinline__ void hash_word(unsigned long long word, int64_t j,
+                                          unsigned long long& t1, unsigned long long& t2) {
+  unsigned long long k1, k2;
+  if (j < kKeyWords) {
+    const ulonglong2 k = __ldg(reinterpret_cast<const ulonglong2*>(&g_hash_keys.k[j][0]));
+    k1 = k.x;
+    k2 = k.y;
+  } else {
+    const unsigned long long step = static_cast<unsigned long long>(j + 1) * kGolden;
+    k1 = sm64_fin(kSeed1 + step);
+    k2 = sm64_fin(kSeed2 + step);
+  }
+  t1 = sm64_fin(word ^ k1);
+  t2 = sm64_fin(word ^ k2);
+}
+
+// ------------------------------------------------------------------------
 // bf16 field arithmetic on packed words (two values per 32-bit word).
 // exponent e = (w >> 7) & 0xFF; sign+mantissa byte s = sign << 7 | mantissa.
 
@@ -268,9 +328,9 @@ __device__ __forceinline__ bool flag_of(const uint32_t* fw, int kb) {
 // ordered by a release store of the status and read after an acquire.
 __device__ __forceinline__ bool flags_in_words(const CompressParams& p) { return p.geo.T <= 32; }
 
-__device__ __forceinline__ void publish(const CompressParams& p, const Tile& x, uint32_t state,
-                                        uint32_t value) {
-  const unsigned long long v = (static_cast<unsigned long long>(p.epoch) << 32) |
+__device__ __forceinline__ void publish(const CompressParams& p, const Tile& x, uint32_t epoch,
+                                        uint32_t state, uint32_t value) {
+  const unsigned long long v = (static_cast<unsigned long long>(epoch) << 32) |
                                (static_cast<unsigned long long>(state) << 30) | value;
   if (flags_in_words(p))
     st_relaxed_u64(&p.tile_status[x.sidx], v);
@@ -284,14 +344,14 @@ __device__ __forceinline__ void publish(const CompressParams& p, const Tile& x, 
 // itself, so it runs while x's own values are still being copied in.  The
 // result is clamped to k0 so that every offset stays in bounds even after a
 // timeout.
-__device__ uint32_t lookback_exclusive(const CompressParams& p, const Tile& x, uint32_t lane,
-                                       bool* timed_out) {
+__device__ uint32_t lookback_exclusive(const CompressParams& p, const Tile& x, uint32_t epoch,
+                                       uint32_t lane, bool* timed_out) {
   if (x.t == 0) {
     *timed_out = false;
     return 0;
   }
   const unsigned long long* st = p.tile_status;
-  const unsigned long long ep = static_cast<unsigned long long>(p.epoch) << 32;
+  const unsigned long long ep = static_cast<unsigned long long>(epoch) << 32;
   const unsigned long long incl = static_cast<unsigned long long>(kStateInclusive) << 30;
   const int64_t gfirst = x.sidx - x.t;
   int64_t base = x.sidx - 1;
@@ -305,7 +365,7 @@ __device__ uint32_t lookback_exclusive(const CompressParams& p, const Tile& x, u
     if (idx >= gfirst) {
       for (;;) {
         v = flags_in_words(p) ? ld_relaxed_u64(&st[idx]) : ld_acquire_u64(&st[idx]);
-        if ((v >> 32) == p.epoch && ((v >> 30) & 3ull) != 0) break;
+        if ((v >> 32) == epoch && ((v >> 30) & 3ull) != 0) break;
         const uint64_t now = globaltimer();
         if (!started) {
           t0 = now;
@@ -354,6 +414,7 @@ __device__ uint32_t lookback_exclusive(const CompressParams& p, const Tile& x, u
 
 struct CompressShared {
   uint32_t ticket;
+  uint32_t epoch; // this launch's tag of look-back and flag words (never 0)
   uint32_t X;     // changed blocks before the tile in its shard
   uint32_t agg;   // changed blocks in the tile
   uint32_t bad;   // a bounded wait ran out on this tile
@@ -387,7 +448,7 @@ __device__ void publish_aggregate(const CompressParams& p, const Tile& x, const 
     if (x.nblk <= 32)
       for (int kb = 0; kb < x.nblk; ++kb) fb[kb] = flag_of(fw, kb) ? 1 : 0;
     if (flags_in_words(p))
-      st_relaxed_u64(&p.tile_flags[x.sidx], (static_cast<unsigned long long>(p.epoch) << 32) | fw[0]);
+      st_relaxed_u64(&p.tile_flags[x.sidx], (static_cast<unsigned long long>(sh.epoch) << 32) | fw[0]);
     uint32_t run = 0;
     for (int i = 0; i < nw; ++i) {
       fpre[i] = run;
@@ -395,7 +456,7 @@ __device__ void publish_aggregate(const CompressParams& p, const Tile& x, const 
     }
     sh.agg = run;
     const bool skip = (p.flags & CIERA_DEBUG_SKIP_FIRST_PUBLISH) && x.t == 0;
-    if (!skip) publish(p, x, x.t == 0 ? kStateInclusive : kStateAggregate, run);
+    if (!skip) publish(p, x, sh.epoch, x.t == 0 ? kStateInclusive : kStateAggregate, run);
   }
   (void)s0;
 }
@@ -440,9 +501,9 @@ __device__ void compress_epilogue(const CompressParams& p, const Tile& x, const 
         if (tj != cur) {
           cur = tj;
           unsigned long long v = ld_relaxed_u64(tf + tj);
-          if ((v >> 32) != p.epoch) {
+          if ((v >> 32) != sh.epoch) {
             const uint64_t t0 = globaltimer();
-            while ((v >> 32) != p.epoch) {
+            while ((v >> 32) != sh.epoch) {
               if (globaltimer() - t0 > p.timeout_ns) {
                 to = true;
                 break;
@@ -473,6 +534,11 @@ __device__ void compress_epilogue(const CompressParams& p, const Tile& x, const 
   }
 }
 
+// kHashed: the change test is the 128-bit block hash against the HashCache
+// (16 bytes per block) instead of an exponent compare against the sender's
+// exponent cache; then only the values are staged, and cs holds nothing but
+// the sign+mantissa bytes of unchanged blocks.  Needs T <= 32.
+template <bool kHashed>
 __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
   extern __shared__ __align__(128) uint8_t dsm[];
   __shared__ CompressShared sh;
@@ -482,27 +548,44 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
   const int64_t B = p.geo.B;
   const int64_t TE = p.geo.T * B;
   const int W = static_cast<int>((p.geo.T + 31) / 32);
+  // flag region: fw[W] | fpre[W] | (kHashed) bsum[2T] hash sums | hs[2T] the
+  // tile's HashCache entries, copied in with the values
+  const int bsum_off = (8 * W + 15) & ~15;
+  const int hs_off = bsum_off + 16 * static_cast<int>(p.geo.T);
+  const int FW = kHashed ? ((hs_off + 16 * static_cast<int>(p.geo.T) + 127) & ~127)
+                         : ((8 * W + 127) & ~127);
   uint32_t* fw = reinterpret_cast<uint32_t*>(dsm);
   uint32_t* fpre = fw + W;
-  uint8_t* ws = dsm + ((8 * W + 127) & ~127);
+  unsigned long long* bsum = reinterpret_cast<unsigned long long*>(dsm + bsum_off);
+  unsigned long long* hs = reinterpret_cast<unsigned long long*>(dsm + hs_off);
+  uint8_t* ws = dsm + FW;
   uint8_t* cs = ws + 2 * TE;
 
   if (tid == 0) {
     // ticket order = start order: a tile only ever waits on tiles whose
     // CTAs started earlier, so the look-back never waits on an unscheduled CTA
-    const uint32_t t = atomicAdd(&p.ctl->ticket, 1u);
-    if (t == gridDim.x - 1) atomicExch(&p.ctl->ticket, 0u);
+    // The counter word holds (launch number << 32) | tickets drawn.  Every
+    // CTA of a launch reads the same launch number with its ticket; the one
+    // that draws the last ticket resets the count and advances the number
+    // in one exchange, so replays of a captured launch get fresh tags too.
+    const unsigned long long v = atomicAdd(&p.ctl->ticket, 1ull);
+    const uint32_t t = static_cast<uint32_t>(v);
+    const uint32_t launch = static_cast<uint32_t>(v >> 32);
+    if (t == gridDim.x - 1) atomicExch(&p.ctl->ticket, static_cast<unsigned long long>(launch + 1u) << 32);
     sh.ticket = t;
+    sh.epoch = launch % 0xffffffffu + 1u;  // 1 .. 2^32-1: a zero-filled word never matches
     sh.bad = 0;
   }
   // the launch must provide the flag words (and the staging of staged
   // tiles); if it does not, report it instead of touching memory past it
-  const uint32_t need = static_cast<uint32_t>(((8 * W + 127) & ~127) + (p.fast ? 3 * TE : 0));
-  if (dynamic_smem_size() < need) {
+  const uint32_t need = static_cast<uint32_t>(FW + (p.fast ? 3 * TE : 0));
+  if (dynamic_smem_size() < need || (kHashed && p.geo.T > 32)) {
     if (tid == 0) record_status(p.ctl, kStatusInternal);
     return;
   }
   for (int i = tid; i < W; i += blockDim.x) fw[i] = 0;
+  if (kHashed)
+    for (int i = tid; i < 2 * p.geo.T; i += blockDim.x) bsum[i] = 0;
   __syncthreads();
   const int64_t g = sh.ticket;
   if (g >= p.geo.total_tiles) {
@@ -524,18 +607,26 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
   const uint16_t* w = p.w + x.shard_off + x.e0;
   uint8_t* c = p.scache + x.shard_off + x.e0;
   const uint32_t te = static_cast<uint32_t>(x.te);
+  const unsigned long long* hc_tile =
+      kHashed ? p.hash_cache + 2 * (static_cast<int64_t>(x.rl) * p.hash_stride + x.k0) : nullptr;
   if (stg && tid == 0) {
     mbar_init(&bar, 1);
     fence_barrier_init();
-    mbar_arrive_expect_tx(&bar, 3u * te);
-    bulk_g2s(ws, w, 2u * te, &bar);
-    bulk_g2s(cs, c, te, &bar);
+    if (kHashed) {
+      mbar_arrive_expect_tx(&bar, 2u * te + 16u * static_cast<uint32_t>(x.nblk));
+      bulk_g2s(ws, w, 2u * te, &bar);
+      bulk_g2s(hs, hc_tile, 16u * static_cast<uint32_t>(x.nblk), &bar);
+    } else {
+      mbar_arrive_expect_tx(&bar, 3u * te);
+      bulk_g2s(ws, w, 2u * te, &bar);
+      bulk_g2s(cs, c, te, &bar);
+    }
   }
   __syncthreads();
 
   if (warp == 0) {
     bool to = false;
-    const uint32_t X = lookback_exclusive(p, x, lane, &to);
+    const uint32_t X = lookback_exclusive(p, x, sh.epoch, lane, &to);
     if (lane == 0) {
       sh.X = X;
       if (to) record_status(p.ctl, kStatusTimeout);
@@ -556,7 +647,91 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
       }
     }
     flaggers_sync();
-    if (cold || sh.bad) {
+    if (kHashed) {
+      // per-block sums of the two seeds' word terms
+      if (stg) {
+        // Each thread sums its groups' terms in registers while they stay in
+        // one block and adds them to the block's sums when it moves on; at
+        // the end a warp whose lanes all sit in one block reduces first.
+        const int ngroups = static_cast<int>(te >> 4);
+        unsigned long long s1 = 0, s2 = 0;
+        int cur = -1;
+        for (int gi = ft; gi < ngroups; gi += kThreads - 32) {
+          const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
+          const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
+          const int64_t v0 = static_cast<int64_t>(gi) << 4;
+          const int kb = static_cast<int>(v0 / B);
+          const int64_t j0 = (v0 - kb * B) >> 3;  // first exponent word of the group
+          const unsigned long long lo =
+              exp4(w0.x, w0.y) | (static_cast<unsigned long long>(exp4(w0.z, w0.w)) << 32);
+          const unsigned long long hi =
+              exp4(w1.x, w1.y) | (static_cast<unsigned long long>(exp4(w1.z, w1.w)) << 32);
+          unsigned long long a1, a2, b1, b2;
+          hash_word(lo, j0, a1, a2);
+          hash_word(hi, j0 + 1, b1, b2);
+          if (kb != cur) {
+            if (cur >= 0) {
+              atomicAdd(&bsum[2 * cur], s1);
+              atomicAdd(&bsum[2 * cur + 1], s2);
+            }
+            s1 = s2 = 0;
+            cur = kb;
+          }
+          s1 += a1 + b1;
+          s2 += a2 + b2;
+        }
+        const int cur0 = __shfl_sync(0xffffffffu, cur, 0);
+        if (__all_sync(0xffffffffu, cur == cur0)) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+            s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+          }
+          if (lane == 0 && cur >= 0) {
+            atomicAdd(&bsum[2 * cur], s1);
+            atomicAdd(&bsum[2 * cur + 1], s2);
+          }
+        } else if (cur >= 0) {
+          atomicAdd(&bsum[2 * cur], s1);
+          atomicAdd(&bsum[2 * cur + 1], s2);
+        }
+      } else {
+        const int64_t wpb = (B + 7) / 8;  // exponent words per block
+        const int64_t nwords = static_cast<int64_t>(x.nblk) * wpb;
+        for (int64_t q = ft; q < nwords; q += kThreads - 32) {
+          const int kb = static_cast<int>(q / wpb);
+          const int64_t j = q - kb * wpb;
+          const int64_t first = kb * B + 8 * j;  // tile-relative
+          const int64_t blen = (kb + 1) * B < x.te ? B : x.te - kb * B;
+          if (8 * j >= blen) continue;
+          unsigned long long word = 0;
+          for (int i = 0; i < 8 && 8 * j + i < blen; ++i)
+            word |= static_cast<unsigned long long>(exp1(w[first + i])) << (8 * i);
+          unsigned long long t1, t2;
+          hash_word(word, j, t1, t2);
+          atomicAdd(&bsum[2 * kb], t1);
+          atomicAdd(&bsum[2 * kb + 1], t2);
+        }
+      }
+      flaggers_sync();
+      // one thread per block: finish both hashes, test and refresh the
+      // HashCache entry
+      for (int kb = ft; kb < x.nblk; kb += kThreads - 32) {
+        const int64_t blen = (kb + 1) * B < x.te ? B : x.te - kb * B;
+        const unsigned long long h1 = sm64_fin(static_cast<unsigned long long>(blen) + bsum[2 * kb]);
+        const unsigned long long h2 =
+            sm64_fin(static_cast<unsigned long long>(blen) + bsum[2 * kb + 1]);
+        unsigned long long* hc = const_cast<unsigned long long*>(hc_tile) + 2 * kb;
+        const unsigned long long o1 = stg ? hs[2 * kb] : hc[0];
+        const unsigned long long o2 = stg ? hs[2 * kb + 1] : hc[1];
+        const bool changed = cold || sh.bad || o1 != h1 || o2 != h2;
+        if (changed) {
+          hc[0] = h1;
+          hc[1] = h2;
+          atomicOr(&fw[kb >> 5], 1u << (kb & 31));
+        }
+      }
+    } else if (cold || sh.bad) {
       for (int kb = ft; kb < x.nblk; kb += kThreads - 32) atomicOr(&fw[kb >> 5], 1u << (kb & 31));
     } else if (stg) {
       const int ngroups = static_cast<int>(te >> 4);
@@ -594,11 +769,13 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
         const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
         const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
         if (flag_of(fw, kb)) {
-          const uint4 e = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w), exp4(w1.x, w1.y),
-                                     exp4(w1.z, w1.w));
-          const uint4 cc = reinterpret_cast<const uint4*>(cs)[gi];
-          if (cold || ((e.x ^ cc.x) | (e.y ^ cc.y) | (e.z ^ cc.z) | (e.w ^ cc.w)))
-            reinterpret_cast<uint4*>(c)[gi] = e;
+          if (!kHashed) {
+            const uint4 e = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w), exp4(w1.x, w1.y),
+                                       exp4(w1.z, w1.w));
+            const uint4 cc = reinterpret_cast<const uint4*>(cs)[gi];
+            if (cold || ((e.x ^ cc.x) | (e.y ^ cc.y) | (e.z ^ cc.z) | (e.w ^ cc.w)))
+              reinterpret_cast<uint4*>(c)[gi] = e;
+          }
         } else {
           reinterpret_cast<uint4*>(cs)[gi] =
               make_uint4(sm4(w0.x, w0.y), sm4(w0.z, w0.w), sm4(w1.x, w1.y), sm4(w1.z, w1.w));
@@ -608,7 +785,7 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
     }
   }
   __syncthreads();
-  if (tid == 0 && x.t > 0) publish(p, x, kStateInclusive, sh.X + sh.agg);
+  if (tid == 0 && x.t > 0) publish(p, x, sh.epoch, kStateInclusive, sh.X + sh.agg);
 
   uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
   if (stg) {
@@ -641,8 +818,10 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
       if (flag_of(fw, kb)) {
         payload[off + 2 * within] = static_cast<uint8_t>(v & 0xFFu);
         payload[off + 2 * within + 1] = static_cast<uint8_t>(v >> 8);
-        const uint8_t e = static_cast<uint8_t>(exp1(v));
-        if (c[j] != e) c[j] = e;
+        if (!kHashed) {
+          const uint8_t e = static_cast<uint8_t>(exp1(v));
+          if (c[j] != e) c[j] = e;
+        }
       } else {
         payload[off + within] = static_cast<uint8_t>(sm1(v));
       }
@@ -915,6 +1094,7 @@ __global__ void __launch_bounds__(kThreads) k_decompress(const DecompressParams 
 // Largest dynamic shared memory already allowed per device and kernel.
 constexpr int kMaxDevices = 64;
 std::atomic<int64_t> g_compress_smem[kMaxDevices];
+std::atomic<int64_t> g_compress_hashed_smem[kMaxDevices];
 std::atomic<int64_t> g_decompress_smem[kMaxDevices];
 
 // Opt the kernel in to `bytes` of dynamic shared memory on the current
@@ -939,12 +1119,19 @@ cudaError_t allow_dynamic_smem(const void* fn, int64_t bytes, std::atomic<int64_
 
 int launch_compress(const CompressParams& p, int64_t smem_bytes, int raw_fixup, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(k_compress), smem_bytes,
-                                     g_compress_smem);
+  const void* fn = p.hashed ? reinterpret_cast<const void*>(k_compress<true>)
+                            : reinterpret_cast<const void*>(k_compress<false>);
+  cudaError_t e =
+      allow_dynamic_smem(fn, smem_bytes, p.hashed ? g_compress_hashed_smem : g_compress_smem);
   if (e != cudaSuccess) return e;
   // one CTA per tile, plus the last ticket (descriptors of empty shards)
   const int64_t grid = p.geo.total_tiles + 1;
-  k_compress<<<static_cast<unsigned>(grid), kThreads, static_cast<size_t>(smem_bytes), s>>>(p);
+  if (p.hashed)
+    k_compress<true>
+        <<<static_cast<unsigned>(grid), kThreads, static_cast<size_t>(smem_bytes), s>>>(p);
+  else
+    k_compress<false>
+        <<<static_cast<unsigned>(grid), kThreads, static_cast<size_t>(smem_bytes), s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (raw_fixup && p.geo.total_tiles > 0) {

@@ -60,10 +60,17 @@ extern "C" int ciera_compress_noalloc(ciera_plan_t plan, int rank_begin, int ran
   const int st = scratch_address(&scratch);
   if (st != CIERA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The array keeps the previous call's contents.  The ticket counter and
-  // the status word must start at zero; the look-back words are tagged with
-  // a per-call epoch and the flag bytes are rewritten before they are read.
-  if (cudaMemsetAsync(scratch, 0, sizeof(ciera::Control), s) != cudaSuccess) return CIERA_E_CUDA;
+  // The array keeps the previous call's contents.  The ticket count (the
+  // low half of the counter word) and the status word must start at zero;
+  // the launch number in the counter's high half must be kept, because the
+  // look-back and flag words are tagged with it, and the flag bytes are
+  // rewritten before they are read.
+  unsigned char* ctl = static_cast<unsigned char*>(scratch);
+  if (cudaMemsetAsync(ctl + offsetof(ciera::Control, ticket), 0, sizeof(uint32_t), s) !=
+          cudaSuccess ||
+      cudaMemsetAsync(ctl + offsetof(ciera::Control, status), 0, sizeof(uint32_t), s) !=
+          cudaSuccess)
+    return CIERA_E_CUDA;
   const int rc = ciera_compress(plan, rank_begin, rank_count, w_dev, sender_cache_dev,
                                 payloads_dev, payload_stride, descs_dev, flags_dev, scratch,
                                 flags, s);

@@ -92,6 +92,19 @@ def lib() -> ctypes.CDLL:
                                             ctypes.c_double, ctypes.c_double, ctypes.c_double,
                                             i64, vp, vp]
             L.oracle_bsc_select.restype = ctypes.c_int
+            u64 = ctypes.c_uint64
+            L.oracle_splitmix64.argtypes = [u64, u64]
+            L.oracle_splitmix64.restype = u64
+            L.oracle_exp_hash64.argtypes = [vp, i64, u64]
+            L.oracle_exp_hash64.restype = u64
+            L.oracle_block_hash128.argtypes = [vp, i64, vp]
+            L.oracle_block_hash128.restype = None
+            L.oracle_compress_shard_hashed.argtypes = [vp, i64, i64, vp, ctypes.c_int, vp, vp,
+                                                       ctypes.POINTER(_Desc)]
+            L.oracle_compress_shard_hashed.restype = ctypes.c_int
+            L.oracle_compress_plan_hashed.argtypes = [vp, i64, i64, i64, vp, ctypes.c_int, vp,
+                                                      i64, vp, vp]
+            L.oracle_compress_plan_hashed.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -233,3 +246,44 @@ def bsc_select(numel, q, world: int, budget_bytes: int, link_Bps=8e9, t_fixed_s=
                                   budget_bytes, link_Bps, t_fixed_s, hbm_Bps, block, _ptr(sel),
                                   _ptr(gain))
     return sel[:n], gain[:n], int(cnt)
+
+
+# ---- hashed sender (Hash128 + HashCache) -------------------------------------
+
+def splitmix64(seed: int, index: int) -> int:
+    """Output number `index` (1-based) of SplitMix64 started at `seed`."""
+    return int(lib().oracle_splitmix64(seed & (2**64 - 1), index))
+
+
+def exp_hash64(exps: np.ndarray, seed: int) -> int:
+    exps = np.ascontiguousarray(exps, dtype=np.uint8)
+    return int(lib().oracle_exp_hash64(_ptr(exps) if exps.size else None, exps.size,
+                                       seed & (2**64 - 1)))
+
+
+def block_hash128(vals: np.ndarray):
+    vals = np.ascontiguousarray(vals, dtype=np.uint16)
+    out = np.zeros(2, dtype=np.uint64)
+    lib().oracle_block_hash128(_ptr(vals) if vals.size else None, vals.size, _ptr(out))
+    return int(out[0]), int(out[1])
+
+
+def compress_plan_hashed(w: np.ndarray, ranks: int, block: int, hash_cache: np.ndarray,
+                         cold: bool, stride: int | None = None):
+    """Sender side for every rank with the hashed change test.  ``hash_cache``
+    (u64[ranks, blocks_per_full_shard, 2]) is updated in place.  Returns
+    (payloads, descs, flags) like compress_plan."""
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    n = w.size
+    s = shard_size(n, ranks) if n else 0
+    if stride is None:
+        stride = max(2 * s, 1)
+    payloads = np.zeros((ranks, stride), dtype=np.uint8)
+    descs = np.zeros(ranks, dtype=DESC_DTYPE)
+    fstride = num_blocks(s, block) if n else 0
+    flags = np.zeros((ranks, max(fstride, 1)), dtype=np.uint8)
+    assert hash_cache.dtype == np.uint64 and hash_cache.size >= 2 * ranks * fstride
+    lib().oracle_compress_plan_hashed(_ptr(w), n, ranks, block, _ptr(hash_cache),
+                                      int(bool(cold)), _ptr(payloads), stride, _ptr(descs),
+                                      _ptr(flags))
+    return payloads, descs, flags[:, :fstride]

@@ -124,51 +124,30 @@ int64_t oracle_bitmap_bytes(int64_t len, int64_t block)
 }
 
 /* ---------------------------------------------------------------------- */
-/* Sender side of Algorithm 1 for one shard.
- *
- *   shard        the shard's bf16 bit patterns (len values)
- *   sender_cache the sender's exponents of this shard from the previous
- *                iteration (len bytes); updated in place
- *   cold         nonzero: no previous exponents exist (reading R4)
- *   payload      output, at least 2*len bytes
- *   flags_out    output, one byte per block, 1 = block changed
- *   d            output descriptor
- * Returns 0.
- */
-int oracle_compress_shard(const uint16_t *shard, int64_t len, int64_t block,
-                          uint8_t *sender_cache, int cold, uint8_t *payload,
-                          uint8_t *flags_out, oracle_desc *d)
+/* Sender side of Algorithm 1, second half: given the per-block flags, write
+ * the payload and the descriptor (readings R3, R4).
+ *   flags   one byte per block, 1 = block changed
+ *   payload output, at least 2*len bytes
+ * Returns 1 if the payload is RAW, 0 if COMPRESSED. */
+static int oracle_build_payload(const uint16_t *shard, int64_t len, int64_t block,
+                                const uint8_t *flags, int cold, uint8_t *payload,
+                                oracle_desc *d)
 {
     int64_t nblocks = oracle_num_blocks(len, block);
     int64_t bm_bytes = oracle_bitmap_bytes(len, block);
     int64_t k, j, pos;
     uint32_t n_changed = 0;
 
-    /* per-block change flag: any exponent differs from the cached one */
     for (k = 0; k < nblocks; ++k) {
-        int64_t lo = k * block;
-        int64_t hi = lo + block < len ? lo + block : len;
-        int changed = 0;
-        if (cold) {
-            changed = 1;
-        } else {
-            for (j = lo; j < hi; ++j) {
-                if (oracle_exp(shard[j]) != sender_cache[j]) {
-                    changed = 1;
-                }
-            }
-        }
-        flags_out[k] = (uint8_t)changed;
-        n_changed += (uint32_t)changed;
+        n_changed += flags[k] ? 1u : 0u;
     }
-
     /* body: blocks in order; changed -> bf16 values, unchanged -> sm bytes */
     pos = 0;
     for (k = 0; k < nblocks; ++k) {
         int64_t lo = k * block;
         int64_t hi = lo + block < len ? lo + block : len;
         for (j = lo; j < hi; ++j) {
-            if (flags_out[k]) {
+            if (flags[k]) {
                 payload[pos] = (uint8_t)(shard[j] & 0xFFu);
                 payload[pos + 1] = (uint8_t)(shard[j] >> 8);
                 pos += 2;
@@ -189,27 +168,67 @@ int oracle_compress_shard(const uint16_t *shard, int64_t len, int64_t block,
         d->mode = ORACLE_RAW;
         d->body_bytes = (uint64_t)(2 * len);
         d->payload_bytes = (uint64_t)(2 * len);
-    } else {
-        /* bitmap after the body: bit k in byte k/8 at position k%8 */
-        for (j = 0; j < bm_bytes; ++j) {
-            payload[pos + j] = 0;
-        }
-        for (k = 0; k < nblocks; ++k) {
-            if (flags_out[k]) {
-                payload[pos + k / 8] |= (uint8_t)(1u << (k % 8));
-            }
-        }
-        d->mode = ORACLE_COMPRESSED;
-        d->body_bytes = (uint64_t)pos;
-        d->payload_bytes = (uint64_t)(pos + bm_bytes);
+        return 1;
     }
+    /* bitmap after the body: bit k in byte k/8 at position k%8 */
+    for (j = 0; j < bm_bytes; ++j) {
+        payload[pos + j] = 0;
+    }
+    for (k = 0; k < nblocks; ++k) {
+        if (flags[k]) {
+            payload[pos + k / 8] |= (uint8_t)(1u << (k % 8));
+        }
+    }
+    d->mode = ORACLE_COMPRESSED;
+    d->body_bytes = (uint64_t)pos;
+    d->payload_bytes = (uint64_t)(pos + bm_bytes);
+    return 0;
+}
 
-    /* HashCache analogue: refresh cached exponents of changed blocks (all
-     * blocks when raw; unchanged blocks already hold equal exponents) */
+/* Sender side of Algorithm 1 for one shard, exact change test (reading R2).
+ *
+ *   shard        the shard's bf16 bit patterns (len values)
+ *   sender_cache the sender's exponents of this shard from the previous
+ *                iteration (len bytes); updated in place
+ *   cold         nonzero: no previous exponents exist (reading R7)
+ *   payload      output, at least 2*len bytes
+ *   flags_out    output, one byte per block, 1 = block changed
+ *   d            output descriptor
+ * Returns 0.
+ */
+int oracle_compress_shard(const uint16_t *shard, int64_t len, int64_t block,
+                          uint8_t *sender_cache, int cold, uint8_t *payload,
+                          uint8_t *flags_out, oracle_desc *d)
+{
+    int64_t nblocks = oracle_num_blocks(len, block);
+    int64_t k, j;
+    int raw;
+
+    /* per-block change flag: any exponent differs from the cached one */
     for (k = 0; k < nblocks; ++k) {
         int64_t lo = k * block;
         int64_t hi = lo + block < len ? lo + block : len;
-        if (flags_out[k] || d->mode == ORACLE_RAW) {
+        int changed = 0;
+        if (cold) {
+            changed = 1;
+        } else {
+            for (j = lo; j < hi; ++j) {
+                if (oracle_exp(shard[j]) != sender_cache[j]) {
+                    changed = 1;
+                }
+            }
+        }
+        flags_out[k] = (uint8_t)changed;
+    }
+
+    raw = oracle_build_payload(shard, len, block, flags_out, cold, payload, d);
+
+    /* refresh cached exponents of changed blocks (all blocks when raw;
+     * unchanged blocks already hold equal exponents) */
+    for (k = 0; k < nblocks; ++k) {
+        int64_t lo = k * block;
+        int64_t hi = lo + block < len ? lo + block : len;
+        if (flags_out[k] || raw) {
             for (j = lo; j < hi; ++j) {
                 sender_cache[j] = (uint8_t)oracle_exp(shard[j]);
             }
@@ -422,4 +441,122 @@ int oracle_bsc_select(const int64_t *numel, const double *q, int n, int world,
     free(order);
     free(ratio);
     return taken;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Section 3.1 / Algorithm 1 (Hash128, HashCache): the paper's sender, which
+ * detects a changed block by a 128-bit hash of its exponents, built from two
+ * independent 64-bit hashes over SplitMix64, instead of an exponent compare.
+ *
+ * SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+ * generators", 2014, with the finalizer used by its public reference code):
+ * state += 0x9e3779b97f4a7c15; z = state;
+ * z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9; z = (z ^ (z >> 27)) * 0x94d049bb133111eb;
+ * output z ^ (z >> 31).
+ *
+ * Reading R14 (how exponents are fed, which seeds):
+ *   word j of a block = its exponents 8j .. 8j+7 as a little-endian 64-bit
+ *   word (positions past the block's end are 0); key_j(seed) = output j+1 of
+ *   SplitMix64 started at state `seed`;
+ *   h(seed) = fin(L + sum_j fin(word_j ^ key_j(seed)))   (sums mod 2^64,
+ *   fin = the finalizer, L = the block's length);
+ *   Hash128 = (h(seed1), h(seed2)) with seed1 = 0x6a09e667f3bcc908 and
+ *   seed2 = 0xbb67ae8584caa73b.
+ * The HashCache holds 16 bytes per block: h(seed1) then h(seed2), each a
+ * little-endian 64-bit word.
+ */
+static uint64_t oracle_sm64_fin(uint64_t z)
+{
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ULL;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebULL;
+    return z ^ (z >> 31);
+}
+
+/* output number `index` (1-based) of SplitMix64 started at `seed` */
+uint64_t oracle_splitmix64(uint64_t seed, uint64_t index)
+{
+    uint64_t state = seed;
+    uint64_t i;
+    for (i = 0; i < index; ++i) {
+        state += 0x9e3779b97f4a7c15ULL;
+    }
+    return oracle_sm64_fin(state);
+}
+
+static const uint64_t ORACLE_SEED1 = 0x6a09e667f3bcc908ULL;
+static const uint64_t ORACLE_SEED2 = 0xbb67ae8584caa73bULL;
+
+/* 64-bit hash of `len` exponent bytes with one seed */
+uint64_t oracle_exp_hash64(const uint8_t *exps, int64_t len, uint64_t seed)
+{
+    int64_t nwords = (len + 7) / 8;
+    int64_t j, i;
+    uint64_t sum = 0;
+    for (j = 0; j < nwords; ++j) {
+        uint64_t word = 0;
+        for (i = 0; i < 8; ++i) {
+            if (8 * j + i < len) {
+                word |= (uint64_t)exps[8 * j + i] << (8 * i);
+            }
+        }
+        sum += oracle_sm64_fin(word ^ oracle_splitmix64(seed, (uint64_t)(j + 1)));
+    }
+    return oracle_sm64_fin((uint64_t)len + sum);
+}
+
+/* Hash128 of one block of bf16 values: exponents first (SplitExpMant) */
+void oracle_block_hash128(const uint16_t *vals, int64_t len, uint64_t out[2])
+{
+    uint8_t *exps = (uint8_t *)malloc((size_t)(len > 0 ? len : 1));
+    int64_t j;
+    for (j = 0; j < len; ++j) {
+        exps[j] = (uint8_t)oracle_exp(vals[j]);
+    }
+    out[0] = oracle_exp_hash64(exps, len, ORACLE_SEED1);
+    out[1] = oracle_exp_hash64(exps, len, ORACLE_SEED2);
+    free(exps);
+}
+
+/* Sender side with the hashed change test (Algorithm 1's sender loop):
+ * block k is changed iff Hash128(block) != HashCache[k] (always on a cold
+ * start); the HashCache entry of a changed block is replaced.  The payload,
+ * flags and descriptor follow the same layout as oracle_compress_shard.
+ * hash_cache: 2 * ceil(len/B) words. */
+int oracle_compress_shard_hashed(const uint16_t *shard, int64_t len, int64_t block,
+                                 uint64_t *hash_cache, int cold, uint8_t *payload,
+                                 uint8_t *flags_out, oracle_desc *d)
+{
+    int64_t nblocks = oracle_num_blocks(len, block);
+    int64_t k;
+    for (k = 0; k < nblocks; ++k) {
+        int64_t lo = k * block;
+        int64_t hi = lo + block < len ? lo + block : len;
+        uint64_t h[2];
+        int changed;
+        oracle_block_hash128(shard + lo, hi - lo, h);
+        changed = cold || h[0] != hash_cache[2 * k] || h[1] != hash_cache[2 * k + 1];
+        flags_out[k] = (uint8_t)changed;
+        if (changed) {
+            hash_cache[2 * k] = h[0];
+            hash_cache[2 * k + 1] = h[1];
+        }
+    }
+    oracle_build_payload(shard, len, block, flags_out, cold, payload, d);
+    return 0;
+}
+
+int oracle_compress_plan_hashed(const uint16_t *w, int64_t n, int64_t ranks, int64_t block,
+                                uint64_t *hash_cache, int cold, uint8_t *payloads,
+                                int64_t stride, oracle_desc *descs, uint8_t *flags_out)
+{
+    int64_t s = oracle_shard_size(n, ranks);
+    int64_t fstride = oracle_num_blocks(s, block);
+    int64_t r;
+    for (r = 0; r < ranks; ++r) {
+        int64_t b = oracle_shard_begin(n, ranks, r);
+        int64_t len = oracle_shard_len(n, ranks, r);
+        oracle_compress_shard_hashed(w + b, len, block, hash_cache + 2 * r * fstride, cold,
+                                     payloads + r * stride, flags_out + r * fstride, &descs[r]);
+    }
+    return 0;
 }

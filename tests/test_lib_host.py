@@ -127,3 +127,12 @@ def test_strerror():
     assert ciera.strerror(ciera.OK) == "ok"
     assert "corrupt" in ciera.strerror(ciera.E_CORRUPT)
     assert "timed out" in ciera.strerror(ciera.E_TIMEOUT)
+
+
+def test_hashed_compress_needs_tiles_of_at_most_32_blocks():
+    L = ciera.lib()
+    p = ciera.Plan(1 << 20, 128, 4)           # 64 blocks per tile
+    cap = p.info.payload_capacity
+    fake = ctypes.c_void_p(4096)              # never dereferenced: the check fails first
+    assert L.ciera_compress_hashed(p.handle, 0, 4, fake, fake, fake, cap, fake, None, fake, 0,
+                                   None) == ciera.E_INVAL
