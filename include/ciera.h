@@ -214,6 +214,47 @@ int ciera_compress_noalloc(ciera_plan_t plan, int rank_begin, int rank_count,
                            int64_t payload_stride, ciera_desc *descs_dev, uint8_t *flags_dev,
                            uint32_t *status_dev, uint32_t flags, void *stream);
 
+/* Computation-communication pipelining on one GPU (Section 3.3): the
+ * sender work of layer i+1 overlaps the receiver work of layer i.
+ *
+ * One layer of a step: the arguments of ciera_compress (all ranks) and of
+ * ciera_decompress for that layer's plan.  A layer's compress and decompress
+ * may share one workspace; different layers must not. */
+typedef struct {
+    ciera_plan_t plan;
+    const uint16_t *w_dev;         /* all ranks' values (sender input) */
+    uint8_t *sender_cache_dev;     /* exponent cache of all ranks */
+    uint8_t *payloads_dev;         /* R payload slots */
+    int64_t payload_stride;
+    ciera_desc *descs_dev;         /* R descriptors */
+    uint8_t *recv_cache_dev;       /* ExpCache, N bytes */
+    uint16_t *out_dev;             /* rebuilt values, N */
+    void *workspace_dev;
+    uint32_t flags;                /* ciera_compress flags of this layer (CIERA_COLD) */
+    uint32_t pad;
+} ciera_layer;
+
+typedef struct ciera_pipeline_s *ciera_pipeline_t;
+
+/* A pipeline for steps of up to max_layers layers: it owns the CUDA events
+ * that order the two streams.  Errors: CIERA_E_INVAL, CIERA_E_CUDA. */
+int ciera_pipeline_create(int max_layers, ciera_pipeline_t *out);
+void ciera_pipeline_destroy(ciera_pipeline_t pipe);
+
+/* Enqueue one step of n layers.  side_stream runs compress(0), compress(1),
+ * ... back to back; `stream` runs decompress(i) as soon as compress(i) has
+ * finished, so compress(i+1) overlaps decompress(i).  The side stream first
+ * waits for everything enqueued on `stream` before the call, and `stream`'s
+ * last decompress waits for all side-stream work, so the whole step is
+ * ordered after earlier work on `stream` and before later work on it, and
+ * can be captured into a CUDA graph from `stream` (replays then reuse the
+ * captured pointers).  Results equal those of ciera_compress and
+ * ciera_decompress called layer by layer.  A pipeline must not be used by
+ * two calls at once.  Errors: CIERA_E_INVAL (n < 1 or > max_layers, equal
+ * streams, bad layer arguments), CIERA_E_CUDA. */
+int ciera_pipeline_step(ciera_pipeline_t pipe, const ciera_layer *layers, int n,
+                        void *stream, void *side_stream);
+
 /* Per-tensor predicate (Section 3.2): 1 = compress, 0 = send raw.
  * With P = N + q*N + ceil(ceil(N/B)/8) expected payload bytes,
  * compress iff (2N - P)/link_Bps > t_fixed_s + (4 + q)*N/hbm_Bps. */

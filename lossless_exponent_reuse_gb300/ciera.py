@@ -50,6 +50,15 @@ class _Info(ctypes.Structure):
         ("fast_path", ctypes.c_int32), ("raw_fixup", ctypes.c_int32)]
 
 
+class _Layer(ctypes.Structure):
+    _fields_ = [("plan", ctypes.c_void_p), ("w_dev", ctypes.c_void_p),
+                ("sender_cache_dev", ctypes.c_void_p), ("payloads_dev", ctypes.c_void_p),
+                ("payload_stride", ctypes.c_int64), ("descs_dev", ctypes.c_void_p),
+                ("recv_cache_dev", ctypes.c_void_p), ("out_dev", ctypes.c_void_p),
+                ("workspace_dev", ctypes.c_void_p), ("flags", ctypes.c_uint32),
+                ("pad", ctypes.c_uint32)]
+
+
 class _CostModel(ctypes.Structure):
     _fields_ = [("link_Bps", ctypes.c_double), ("q_hat", ctypes.c_double),
                 ("t_fixed_s", ctypes.c_double), ("hbm_Bps", ctypes.c_double),
@@ -70,6 +79,9 @@ SIGNATURES = {
                                      _vp]),
     "ciera_compress_noalloc": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _u32,
                                       _vp]),
+    "ciera_pipeline_create": (_i32, [_i32, ctypes.POINTER(_vp)]),
+    "ciera_pipeline_destroy": (None, [_vp]),
+    "ciera_pipeline_step": (_i32, [_vp, _vp, _i32, _vp, _vp]),
     "ciera_status": (_i32, [_vp, _vp]),
     "ciera_should_compress": (_i32, [_i64]),
     "ciera_bsc_select": (_i32, [_vp, _vp, _i32, _i32, _i64, _vp, _vp]),
@@ -315,3 +327,42 @@ def decode_descs(descs: torch.Tensor) -> list:
         mode, nch, body, pay = struct.unpack_from("<IIQQ", raw, i * DESC_BYTES)
         out.append(dict(mode=mode, n_changed_blocks=nch, body_bytes=body, payload_bytes=pay))
     return out
+
+
+class Pipeline:
+    """ciera_pipeline_*: steps over several layers' simulated Allgathers with
+    compress(i+1) on a side stream overlapping decompress(i)."""
+
+    def __init__(self, max_layers: int):
+        h = ctypes.c_void_p()
+        _check(lib().ciera_pipeline_create(int(max_layers), ctypes.byref(h)),
+               "ciera_pipeline_create")
+        self._h = h
+        self.max_layers = max_layers
+        self.side = torch.cuda.Stream()
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and _lib is not None:
+            _lib.ciera_pipeline_destroy(h)
+            self._h = None
+
+    def step(self, layers, inputs, stream=None) -> None:
+        """layers: SimulatedAllgather objects (exact sender); inputs: their
+        weights for this step.  Advances each layer's iteration count."""
+        arr = (_Layer * len(layers))()
+        for i, (ag, w) in enumerate(zip(layers, inputs)):
+            if ag.hashed:
+                raise ValueError("the pipeline drives the exact sender")
+            arr[i] = _Layer(ag.plan.handle.value, _dev_ptr(w, "w", torch.uint16),
+                            _dev_ptr(ag.sender_cache, "sender_cache", torch.uint8),
+                            _dev_ptr(ag.payloads, "payloads", torch.uint8),
+                            ag.payloads.stride(0), _dev_ptr(ag.descs, "descs", torch.uint8),
+                            _dev_ptr(ag.recv_cache, "recv_cache", torch.uint8),
+                            _dev_ptr(ag.out, "out", torch.uint16),
+                            _dev_ptr(ag.workspace, "workspace", torch.uint8),
+                            COLD if ag.iteration == 0 else 0, 0)
+        _check(lib().ciera_pipeline_step(self._h, arr, len(layers), _stream_handle(stream),
+                                         self.side.cuda_stream), "ciera_pipeline_step")
+        for ag in layers:
+            ag.iteration += 1

@@ -244,6 +244,70 @@ int ciera_compress_hashed(ciera_plan_t p, int rank_begin, int rank_count, const 
                        stream);
 }
 
+}  // extern "C"
+
+struct ciera_pipeline_s {
+  int max_layers;
+  cudaEvent_t fork;
+  std::vector<cudaEvent_t> done;  // compress(i) finished
+};
+
+extern "C" {
+
+int ciera_pipeline_create(int max_layers, ciera_pipeline_t* out) {
+  if (!out || max_layers < 1) return CIERA_E_INVAL;
+  ciera_pipeline_s* pp = new (std::nothrow) ciera_pipeline_s();
+  if (!pp) return CIERA_E_INVAL;
+  pp->max_layers = max_layers;
+  pp->done.assign(static_cast<size_t>(max_layers), nullptr);
+  bool ok = cudaEventCreateWithFlags(&pp->fork, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; ok && i < max_layers; ++i)
+    ok = cudaEventCreateWithFlags(&pp->done[i], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    ciera_pipeline_destroy(pp);
+    return CIERA_E_CUDA;
+  }
+  *out = pp;
+  return CIERA_OK;
+}
+
+void ciera_pipeline_destroy(ciera_pipeline_t pp) {
+  if (!pp) return;
+  if (pp->fork) cudaEventDestroy(pp->fork);
+  for (cudaEvent_t e : pp->done)
+    if (e) cudaEventDestroy(e);
+  delete pp;
+}
+
+int ciera_pipeline_step(ciera_pipeline_t pp, const ciera_layer* layers, int n, void* stream,
+                        void* side_stream) {
+  if (!pp || !layers || n < 1 || n > pp->max_layers || stream == side_stream)
+    return CIERA_E_INVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStream_t side = static_cast<cudaStream_t>(side_stream);
+  // fork: the side stream starts after what is already queued on `stream`
+  if (cudaEventRecord(pp->fork, s) != cudaSuccess ||
+      cudaStreamWaitEvent(side, pp->fork, 0) != cudaSuccess)
+    return CIERA_E_CUDA;
+  for (int i = 0; i < n; ++i) {
+    const ciera_layer& L = layers[i];
+    if (!L.plan) return CIERA_E_INVAL;
+    int rc = ciera_compress(L.plan, 0, static_cast<int>(L.plan->ranks), L.w_dev,
+                            L.sender_cache_dev, L.payloads_dev, L.payload_stride, L.descs_dev,
+                            nullptr, L.workspace_dev, L.flags, side);
+    if (rc != CIERA_OK) return rc;
+    if (cudaEventRecord(pp->done[i], side) != cudaSuccess ||
+        cudaStreamWaitEvent(s, pp->done[i], 0) != cudaSuccess)
+      return CIERA_E_CUDA;
+    rc = ciera_decompress(L.plan, L.payloads_dev, L.payload_stride, L.descs_dev,
+                          L.recv_cache_dev, L.out_dev, L.workspace_dev, 0, s);
+    if (rc != CIERA_OK) return rc;
+  }
+  // join: the last decompress already waits for the last compress, and the
+  // side stream does nothing after it
+  return CIERA_OK;
+}
+
 int ciera_decompress(ciera_plan_t p, const uint8_t* payloads_dev, int64_t payload_stride,
                      const ciera_desc* descs_dev, uint8_t* recv_cache_dev, uint16_t* out_dev,
                      void* workspace_dev, uint32_t flags, void* stream) {
