@@ -176,3 +176,21 @@ def test_cache_invariants_and_round_trip_on_workload_2_shape_slice():
     w_last = torch.from_numpy(seq[-1].view(np.int16)).cuda().view(torch.uint16)
     assert torch.equal(ag.recv_cache, exps_dev(w_last))
     assert torch.equal(ag.sender_cache, exps_dev(w_last))
+
+
+def test_host_streamer_round_trips_every_step():
+    # weights from pinned host memory, rebuilt weights back, overlapped
+    from lossless_exponent_reuse_gb300.allgather import HostStreamer
+    n, R, B = 131072, 4, 256
+    seq = edge_sequence(n, B, seed=21)
+    ag = SimulatedAllgather(n, B, R)
+    hs = HostStreamer(ag)
+    host = [torch.from_numpy(w.view(np.int16)).pin_memory() for w in seq]
+    outs = [torch.empty(n, dtype=torch.int16).pin_memory() for _ in seq]
+    for w, o in zip(host, outs):
+        hs.step(w, o)
+    hs.finish()
+    torch.cuda.synchronize()
+    assert ag.status() == ciera.OK
+    for w, o in zip(host, outs):
+        assert torch.equal(w, o)
