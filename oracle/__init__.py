@@ -105,6 +105,18 @@ def lib() -> ctypes.CDLL:
             L.oracle_compress_plan_hashed.argtypes = [vp, i64, i64, i64, vp, ctypes.c_int, vp,
                                                       i64, vp, vp]
             L.oracle_compress_plan_hashed.restype = ctypes.c_int
+            L.oracle_rans_table.argtypes = [vp, vp]
+            L.oracle_rans_table.restype = None
+            L.oracle_rans_encode_block.argtypes = [vp, i64, vp, vp]
+            L.oracle_rans_encode_block.restype = i64
+            L.oracle_rans_decode_block.argtypes = [vp, i64, i64, vp, vp]
+            L.oracle_rans_decode_block.restype = ctypes.c_int
+            L.oracle_compress_shard_rans.argtypes = [vp, i64, i64, vp, ctypes.c_int, vp, vp, vp,
+                                                     vp, ctypes.POINTER(_Desc)]
+            L.oracle_compress_shard_rans.restype = ctypes.c_int
+            L.oracle_decompress_shard_rans.argtypes = [vp, ctypes.POINTER(_Desc), i64, i64, vp,
+                                                       vp]
+            L.oracle_decompress_shard_rans.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -287,3 +299,65 @@ def compress_plan_hashed(w: np.ndarray, ranks: int, block: int, hash_cache: np.n
                                       int(bool(cold)), _ptr(payloads), stride, _ptr(descs),
                                       _ptr(flags))
     return payloads, descs, flags[:, :fstride]
+
+
+# ---- rANS-coded changed exponents (RANS payloads) ----------------------------
+
+RANS = 2
+
+
+def rans_table(hist) -> np.ndarray:
+    hist = np.ascontiguousarray(hist, dtype=np.uint32)
+    assert hist.size == 256
+    freq = np.zeros(256, dtype=np.uint16)
+    lib().oracle_rans_table(_ptr(hist), _ptr(freq))
+    return freq
+
+
+def rans_encode_block(exps: np.ndarray, freq: np.ndarray) -> np.ndarray:
+    exps = np.ascontiguousarray(exps, dtype=np.uint8)
+    freq = np.ascontiguousarray(freq, dtype=np.uint16)
+    L = exps.size
+    rec = np.zeros(64 + 32 * (4 + 2 * ((L + 31) // 32)) + 16, dtype=np.uint8)
+    size = lib().oracle_rans_encode_block(_ptr(exps) if L else None, L, _ptr(freq), _ptr(rec))
+    return rec[:size].copy()
+
+
+def rans_decode_block(rec: np.ndarray, L: int, freq: np.ndarray):
+    rec = np.ascontiguousarray(rec, dtype=np.uint8)
+    freq = np.ascontiguousarray(freq, dtype=np.uint16)
+    out = np.zeros(max(L, 1), dtype=np.uint8)
+    st = lib().oracle_rans_decode_block(_ptr(rec), rec.size, L, _ptr(freq), _ptr(out))
+    return int(st), out[:L]
+
+
+def compress_shard_rans(shard, block, sender_cache, cold, hist_prev):
+    """RANS sender for one shard.  Updates ``sender_cache``.  Returns
+    (payload, flags, desc, hist_cur)."""
+    shard = np.ascontiguousarray(shard, dtype=np.uint16)
+    n = shard.size
+    hist_prev = np.ascontiguousarray(hist_prev, dtype=np.uint32)
+    hist_cur = np.zeros(256, dtype=np.uint32)
+    payload = np.zeros(max(2 * n, 1), dtype=np.uint8)
+    flags = np.zeros(max(num_blocks(n, block), 1), dtype=np.uint8)
+    d = _Desc()
+    lib().oracle_compress_shard_rans(_ptr(shard), n, block, _ptr(sender_cache), int(bool(cold)),
+                                     _ptr(hist_prev), _ptr(hist_cur), _ptr(payload), _ptr(flags),
+                                     ctypes.byref(d))
+    desc = dict(mode=d.mode, n_changed_blocks=d.n_changed_blocks, body_bytes=d.body_bytes,
+                payload_bytes=d.payload_bytes)
+    return payload[:d.payload_bytes].copy(), flags[:num_blocks(n, block)].copy(), desc, hist_cur
+
+
+def decompress_shard_any(payload, desc, length, block, recv_cache):
+    """Receiver for one shard, any mode (RAW, COMPRESSED, RANS)."""
+    if desc["mode"] != RANS:
+        return decompress_shard(payload, desc, length, block, recv_cache)
+    buf = np.ascontiguousarray(payload, dtype=np.uint8)
+    if buf.size == 0:
+        buf = np.zeros(1, np.uint8)
+    out = np.zeros(max(length, 1), dtype=np.uint16)
+    d = _Desc(desc["mode"], desc["n_changed_blocks"], desc["body_bytes"], desc["payload_bytes"])
+    st = lib().oracle_decompress_shard_rans(_ptr(buf), ctypes.byref(d), length, block,
+                                            _ptr(recv_cache), _ptr(out))
+    return int(st), out[:length].copy()

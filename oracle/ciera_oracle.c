@@ -560,3 +560,334 @@ int oracle_compress_plan_hashed(const uint16_t *w, int64_t n, int64_t ranks, int
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------------- */
+/* Section 3.1: "the exponents that are changed" entropy-coded with ANS.  An
+ * own range variant of ANS (rANS; Duda, "Asymmetric numeral systems",
+ * arXiv:1311.2540), reading R15:
+ *   - probability precision 12 bits (frequencies sum to 4096), 32-bit state
+ *     kept in [2^16, 2^32), renormalised 16 bits at a time;
+ *   - a block's exponents are coded as 32 interleaved lanes: lane l codes
+ *     positions l, l+32, l+64, ... of the block;
+ *   - encoding runs over a lane's symbols backwards; the lane's stream, in
+ *     the order the decoder reads it, is the final state (high 16 bits, then
+ *     low 16 bits) followed by the renormalisation words, last emitted first;
+ *   - a block's record: 32 uint16 lane word counts, then the lanes' words
+ *     (uint16, little-endian) in lane order, zero-padded to 16 bytes;
+ *   - the frequency table of a shard comes from a histogram h of exponents:
+ *     f[s] = 1 + floor(h[s] * 3840 / sum(h)), the rest of 4096 added to the
+ *     most frequent symbol (lowest s on a tie); all 16 if h is empty.
+ */
+enum { ORACLE_RANS_BITS = 12, ORACLE_RANS_TOTAL = 4096, ORACLE_RANS_LANES = 32 };
+static const uint32_t ORACLE_RANS_LOW = 1u << 16;
+
+void oracle_rans_table(const uint32_t *hist, uint16_t *freq)
+{
+    uint64_t total = 0;
+    uint32_t sum = 0;
+    int s, best = 0;
+    for (s = 0; s < 256; ++s) {
+        total += hist[s];
+    }
+    if (total == 0) {
+        for (s = 0; s < 256; ++s) {
+            freq[s] = 16;
+        }
+        return;
+    }
+    for (s = 0; s < 256; ++s) {
+        freq[s] = (uint16_t)(1 + (uint64_t)hist[s] * 3840u / total);
+        sum += freq[s];
+        if (hist[s] > hist[best]) {
+            best = s;
+        }
+    }
+    freq[best] = (uint16_t)(freq[best] + (ORACLE_RANS_TOTAL - sum));
+}
+
+static void oracle_rans_cum(const uint16_t *freq, uint32_t *cum)
+{
+    int s;
+    cum[0] = 0;
+    for (s = 0; s < 256; ++s) {
+        cum[s + 1] = cum[s] + freq[s];
+    }
+}
+
+/* Record of one block of L exponents; returns its size in bytes (a multiple
+ * of 16).  rec needs 64 + 32 * (4 + 2 * ceil(L/32)) + 16 bytes. */
+int64_t oracle_rans_encode_block(const uint8_t *exps, int64_t L, const uint16_t *freq,
+                                 uint8_t *rec)
+{
+    uint32_t cum[257];
+    int64_t per_lane = (L + ORACLE_RANS_LANES - 1) / ORACLE_RANS_LANES;
+    uint16_t *tmp = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(per_lane + 2));
+    int64_t pos = 2 * ORACLE_RANS_LANES;  /* after the header */
+    int lane;
+    oracle_rans_cum(freq, cum);
+    for (lane = 0; lane < ORACLE_RANS_LANES; ++lane) {
+        uint64_t x = ORACLE_RANS_LOW;
+        int64_t nw = 0, j, i;
+        int64_t last = -1;
+        for (j = lane; j < L; j += ORACLE_RANS_LANES) {
+            last = j;
+        }
+        for (j = last; j >= 0; j -= ORACLE_RANS_LANES) {
+            uint32_t sym = exps[j];
+            uint64_t f = freq[sym];
+            uint64_t x_max = f << 20;  /* ((2^16 >> 12) << 16) * f */
+            if (x >= x_max) {
+                tmp[nw++] = (uint16_t)(x & 0xFFFFu);
+                x >>= 16;
+            }
+            x = ((x / f) << ORACLE_RANS_BITS) + (x % f) + cum[sym];
+        }
+        tmp[nw++] = (uint16_t)(x & 0xFFFFu);
+        tmp[nw++] = (uint16_t)(x >> 16);
+        /* header: this lane's word count */
+        rec[2 * lane] = (uint8_t)(nw & 0xFF);
+        rec[2 * lane + 1] = (uint8_t)(nw >> 8);
+        /* stream in decoding order: the words in reverse order of emission */
+        for (i = nw - 1; i >= 0; --i) {
+            rec[pos] = (uint8_t)(tmp[i] & 0xFF);
+            rec[pos + 1] = (uint8_t)(tmp[i] >> 8);
+            pos += 2;
+        }
+    }
+    free(tmp);
+    while (pos % 16) {
+        rec[pos++] = 0;
+    }
+    return pos;
+}
+
+/* Decode one record into L exponents.  rec_bytes bounds every read.
+ * Returns 0, or -1 for a record that does not decode cleanly. */
+int oracle_rans_decode_block(const uint8_t *rec, int64_t rec_bytes, int64_t L,
+                             const uint16_t *freq, uint8_t *exps)
+{
+    uint32_t cum[257];
+    int64_t base = 2 * ORACLE_RANS_LANES;
+    int lane;
+    oracle_rans_cum(freq, cum);
+    if (rec_bytes < base) {
+        return -1;
+    }
+    for (lane = 0; lane < ORACLE_RANS_LANES; ++lane) {
+        int64_t nw = rec[2 * lane] | (rec[2 * lane + 1] << 8);
+        int64_t idx = 0, j;
+        uint64_t x;
+        const uint8_t *w = rec + base;
+        if (nw < 2 || base + 2 * nw > rec_bytes) {
+            return -1;
+        }
+        x = ((uint64_t)(w[0] | (w[1] << 8)) << 16) | (uint64_t)(w[2] | (w[3] << 8));
+        idx = 2;
+        for (j = lane; j < L; j += ORACLE_RANS_LANES) {
+            uint32_t slot = (uint32_t)(x & (ORACLE_RANS_TOTAL - 1));
+            uint32_t sym = 0;
+            while (cum[sym + 1] <= slot) {
+                ++sym;
+            }
+            exps[j] = (uint8_t)sym;
+            x = (uint64_t)freq[sym] * (x >> ORACLE_RANS_BITS) + slot - cum[sym];
+            if (x < ORACLE_RANS_LOW) {
+                if (idx >= nw) {
+                    return -1;
+                }
+                x = (x << 16) | (uint64_t)(w[2 * idx] | (w[2 * idx + 1] << 8));
+                ++idx;
+            }
+        }
+        if (idx != nw || x != ORACLE_RANS_LOW) {
+            return -1;
+        }
+        base += 2 * nw;
+    }
+    return 0;
+}
+
+/* RANS payload of one shard (reading R15):
+ *   [0, len)             sign+mantissa byte of every value
+ *   A = align16(len)     bitmap, ceil(n_b/8) bytes
+ *   C = align16(A + bm)  frequency table, 256 uint16
+ *   O = C + 512          record offset of every block, uint32 (relative to D;
+ *                        0 for an unchanged block)
+ *   D = align16(O + 4 n_b)  the records of the changed blocks, in order
+ * Descriptor: mode 2, body_bytes = D, payload_bytes = D + records.  RAW as
+ * before when cold, empty, or when the payload would not be smaller than
+ * 2*len.  hist_prev: histogram of the shard's exponents one iteration
+ * earlier (the table's source); hist_cur: output, this iteration's. */
+int oracle_compress_shard_rans(const uint16_t *shard, int64_t len, int64_t block,
+                               uint8_t *sender_cache, int cold, const uint32_t *hist_prev,
+                               uint32_t *hist_cur, uint8_t *payload, uint8_t *flags_out,
+                               oracle_desc *d)
+{
+    int64_t nblocks = oracle_num_blocks(len, block);
+    int64_t bm = oracle_bitmap_bytes(len, block);
+    int64_t A = (len + 15) / 16 * 16;
+    int64_t C = (A + bm + 15) / 16 * 16;
+    int64_t O = C + 512;
+    int64_t D = (O + 4 * nblocks + 15) / 16 * 16;
+    int64_t pos = 0, k, j;
+    uint16_t freq[256];
+    uint8_t *exps = (uint8_t *)malloc((size_t)(block > 0 ? block : 1));
+    uint8_t *rec = (uint8_t *)malloc((size_t)(64 + 32 * (4 + 2 * ((block + 31) / 32)) + 16));
+    int raw;
+    uint8_t *tmp = (uint8_t *)malloc((size_t)(2 * len > 0 ? 2 * len : 1));
+
+    for (j = 0; j < 256; ++j) {
+        hist_cur[j] = 0;
+    }
+    for (j = 0; j < len; ++j) {
+        hist_cur[oracle_exp(shard[j])] += 1;
+    }
+    /* flags: the exact change test */
+    for (k = 0; k < nblocks; ++k) {
+        int64_t lo = k * block;
+        int64_t hi = lo + block < len ? lo + block : len;
+        int changed = cold;
+        for (j = lo; j < hi && !changed; ++j) {
+            if (oracle_exp(shard[j]) != sender_cache[j]) {
+                changed = 1;
+            }
+        }
+        flags_out[k] = (uint8_t)changed;
+    }
+    oracle_rans_table(hist_prev, freq);
+    /* build the RANS layout in tmp (2*len bytes); it becomes the payload
+     * only if it ends up smaller than the raw shard */
+    raw = cold || len == 0 || D >= 2 * len;
+    if (!raw) {
+        uint32_t n_changed = 0;
+        memset(tmp, 0, (size_t)D);
+        for (j = 0; j < len; ++j) {
+            tmp[j] = (uint8_t)oracle_sm(shard[j]);
+        }
+        for (k = 0; k < nblocks; ++k) {
+            if (flags_out[k]) {
+                tmp[A + k / 8] |= (uint8_t)(1u << (k % 8));
+            }
+        }
+        for (j = 0; j < 256; ++j) {
+            tmp[C + 2 * j] = (uint8_t)(freq[j] & 0xFF);
+            tmp[C + 2 * j + 1] = (uint8_t)(freq[j] >> 8);
+        }
+        pos = D;
+        for (k = 0; k < nblocks; ++k) {
+            int64_t lo = k * block;
+            int64_t hi = lo + block < len ? lo + block : len;
+            int64_t size;
+            if (!flags_out[k]) {
+                continue;
+            }
+            ++n_changed;
+            for (j = lo; j < hi; ++j) {
+                exps[j - lo] = (uint8_t)oracle_exp(shard[j]);
+            }
+            size = oracle_rans_encode_block(exps, hi - lo, freq, rec);
+            if (pos + size >= 2 * len) {
+                raw = 1;
+                break;
+            }
+            for (j = 0; j < 4; ++j) {
+                tmp[O + 4 * k + j] = (uint8_t)(((uint64_t)(pos - D) >> (8 * j)) & 0xFF);
+            }
+            memcpy(tmp + pos, rec, (size_t)size);
+            pos += size;
+        }
+        if (!raw) {
+            memcpy(payload, tmp, (size_t)pos);
+            d->mode = 2;
+            d->n_changed_blocks = n_changed;
+            d->body_bytes = (uint64_t)D;
+            d->payload_bytes = (uint64_t)pos;
+        }
+    }
+    if (raw) {
+        uint32_t n_changed = 0;
+        for (k = 0; k < nblocks; ++k) {
+            n_changed += flags_out[k];
+        }
+        for (j = 0; j < len; ++j) {
+            payload[2 * j] = (uint8_t)(shard[j] & 0xFFu);
+            payload[2 * j + 1] = (uint8_t)(shard[j] >> 8);
+        }
+        d->mode = ORACLE_RAW;
+        d->n_changed_blocks = n_changed;
+        d->body_bytes = (uint64_t)(2 * len);
+        d->payload_bytes = (uint64_t)(2 * len);
+    }
+    for (k = 0; k < nblocks; ++k) {
+        int64_t lo = k * block;
+        int64_t hi = lo + block < len ? lo + block : len;
+        if (flags_out[k] || raw) {
+            for (j = lo; j < hi; ++j) {
+                sender_cache[j] = (uint8_t)oracle_exp(shard[j]);
+            }
+        }
+    }
+    free(exps);
+    free(rec);
+    free(tmp);
+    return 0;
+}
+
+/* Receiver of a RANS payload (mode 2).  Returns 0, or -1 if the payload does
+ * not decode cleanly against the descriptor. */
+int oracle_decompress_shard_rans(const uint8_t *payload, const oracle_desc *d, int64_t len,
+                                 int64_t block, uint8_t *recv_cache, uint16_t *out)
+{
+    int64_t nblocks = oracle_num_blocks(len, block);
+    int64_t bm = oracle_bitmap_bytes(len, block);
+    int64_t A = (len + 15) / 16 * 16;
+    int64_t C = (A + bm + 15) / 16 * 16;
+    int64_t O = C + 512;
+    int64_t D = (O + 4 * nblocks + 15) / 16 * 16;
+    int64_t k, j;
+    uint16_t freq[256];
+    uint32_t sum = 0, seen = 0;
+    uint8_t *exps = (uint8_t *)malloc((size_t)(block > 0 ? block : 1));
+    if (d->mode != 2 || d->body_bytes != (uint64_t)D || d->payload_bytes < (uint64_t)D) {
+        free(exps);
+        return -1;
+    }
+    for (j = 0; j < 256; ++j) {
+        freq[j] = (uint16_t)(payload[C + 2 * j] | (payload[C + 2 * j + 1] << 8));
+        if (freq[j] == 0) {
+            free(exps);
+            return -1;
+        }
+        sum += freq[j];
+    }
+    if (sum != ORACLE_RANS_TOTAL) {
+        free(exps);
+        return -1;
+    }
+    for (k = 0; k < nblocks; ++k) {
+        int64_t lo = k * block;
+        int64_t hi = lo + block < len ? lo + block : len;
+        int changed = (payload[A + k / 8] >> (k % 8)) & 1;
+        if (changed) {
+            uint64_t off = 0;
+            ++seen;
+            for (j = 0; j < 4; ++j) {
+                off |= (uint64_t)payload[O + 4 * k + j] << (8 * j);
+            }
+            if (D + off >= d->payload_bytes ||
+                oracle_rans_decode_block(payload + D + off, (int64_t)(d->payload_bytes - D - off),
+                                         hi - lo, freq, exps) != 0) {
+                free(exps);
+                return -1;
+            }
+            for (j = lo; j < hi; ++j) {
+                recv_cache[j] = exps[j - lo];
+            }
+        }
+        for (j = lo; j < hi; ++j) {
+            out[j] = (uint16_t)oracle_join(payload[j], recv_cache[j]);
+        }
+    }
+    free(exps);
+    return seen == d->n_changed_blocks ? 0 : -1;
+}
