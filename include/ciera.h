@@ -70,9 +70,12 @@ extern "C" {
 
 #define CIERA_MODE_COMPRESSED 0u
 #define CIERA_MODE_RAW 1u
+#define CIERA_MODE_RANS 2u       /* ciera_compress_rans: exponents of changed blocks rANS-coded */
 
 /* ciera_compress flags */
 #define CIERA_COLD 1u            /* no previous exponents: every block changed, payload raw */
+/* ciera_decompress flags */
+#define CIERA_DECOMPRESS_RANS 1u /* also accept CIERA_MODE_RANS payloads */
 /* Test hook: the first tile of every shard never publishes its prefix, so
  * that the tiles after it run into the bounded wait (CIERA_E_TIMEOUT). */
 #define CIERA_DEBUG_SKIP_FIRST_PUBLISH 0x80000000u
@@ -81,7 +84,7 @@ typedef struct ciera_plan_s *ciera_plan_t;
 
 /* Descriptor of one rank's payload, device-resident, 24 bytes. */
 typedef struct {
-    uint32_t mode;             /* CIERA_MODE_COMPRESSED or CIERA_MODE_RAW */
+    uint32_t mode;             /* CIERA_MODE_COMPRESSED, CIERA_MODE_RAW or CIERA_MODE_RANS */
     uint32_t n_changed_blocks; /* blocks whose exponents changed (all on a cold start) */
     uint64_t body_bytes;       /* bytes before the bitmap (2*len when raw) */
     uint64_t payload_bytes;    /* total bytes to send (body + bitmap, or 2*len) */
@@ -172,15 +175,58 @@ int ciera_compress_hashed(ciera_plan_t plan, int rank_begin, int rank_count,
                           int64_t payload_stride, ciera_desc *descs_dev, uint8_t *flags_dev,
                           void *workspace_dev, uint32_t flags, void *stream);
 
+/* Sender side with the changed exponents entropy-coded (Section 3.1: the
+ * sign+mantissa bytes go out as they are, the exponents that changed are
+ * coded with ANS).  Change test, flags and sender cache as ciera_compress;
+ * the payload of a shard of len values and n_b blocks is CIERA_MODE_RANS:
+ *   [0, len)        sign+mantissa byte of every value, in order
+ *   A = align16(len)                  bitmap, as in COMPRESSED payloads
+ *   C = align16(A + ceil(n_b/8))      frequency table: 256 uint16, each >= 1,
+ *                                     summing to 4096
+ *   O = C + 512     n_b + 1 uint32: entry k = bytes of the records of the
+ *                   blocks before k; entry n_b = all records' bytes
+ *   D = align16(O + 4 (n_b + 1))      the records of the changed blocks
+ * with zero bytes in the alignment gaps; body_bytes = D, payload_bytes = D +
+ * records.  A block's record codes its L exponents with rANS (12-bit
+ * probabilities, 32-bit state in [2^16, 2^32), 16-bit renormalisation) as
+ * 32 interleaved lanes, lane l holding positions l, l+32, ...: 32 uint16
+ * lane word counts, then each lane's words in decoding order (final state,
+ * high half first, then the renormalisation words, last emitted first),
+ * zero-padded to 16 bytes.  Frequencies f[s] = 1 + floor(h[s]*3840/sum h),
+ * the rest of 4096 added to the most frequent symbol (lowest on a tie),
+ * all 16 when h is empty, from h = hist_prev's row of the rank.  RAW as in
+ * ciera_compress when cold, or when the RANS payload would not be smaller
+ * than 2*len.
+ *   hist_prev_dev  rank_count rows of 256 uint32: the histogram of each
+ *                  shard's exponents one call earlier (zeros at first)
+ *   hist_out_dev   rank_count rows of 256 uint32, overwritten with the
+ *                  histogram of this call's exponents (the next call's
+ *                  hist_prev); must not overlap hist_prev_dev
+ * Other arguments as ciera_compress.  Errors: as ciera_compress, and
+ * CIERA_E_INVAL unless the plan takes the fast path, N is a multiple of 16,
+ * S <= 2^30, and w_dev, sender_cache_dev, payloads_dev (and the stride) are
+ * 16-byte aligned and the histograms 4-byte aligned. */
+int ciera_compress_rans(ciera_plan_t plan, int rank_begin, int rank_count, const uint16_t *w_dev,
+                        uint8_t *sender_cache_dev, const uint32_t *hist_prev_dev,
+                        uint32_t *hist_out_dev, uint8_t *payloads_dev, int64_t payload_stride,
+                        ciera_desc *descs_dev, uint8_t *flags_dev, void *workspace_dev,
+                        uint32_t flags, void *stream);
+
 /* Receiver side (Section 3.1; Algorithm 1, receiver): rebuilds all N values
  * from the R payloads and refreshes the receiver's exponent cache.
  *   payloads_dev   R payloads, rank r's at payloads_dev + r*payload_stride
  *   descs_dev      R descriptors (device memory)
  *   recv_cache_dev N exponent bytes (ExpCache); updated in place
  *   out_dev        N bf16 outputs
- * A rank whose descriptor or bitmap does not match the plan is skipped (its
- * output range is left untouched) and CIERA_E_CORRUPT is recorded for
- * ciera_status().  Errors: CIERA_E_INVAL, CIERA_E_CUDA. */
+ *   flags          0, or CIERA_DECOMPRESS_RANS to accept CIERA_MODE_RANS
+ *                  payloads as well (then the plan must take the fast path,
+ *                  N be a multiple of 16 and every pointer be 16-byte
+ *                  aligned, else CIERA_E_INVAL)
+ * A rank whose descriptor, bitmap or frequency table does not match the
+ * plan is skipped (its output range is left untouched) and CIERA_E_CORRUPT
+ * is recorded for ciera_status(); so is a RANS record that does not decode
+ * cleanly (that rank's output is then undefined).  Errors: CIERA_E_INVAL,
+ * CIERA_E_CUDA. */
 int ciera_decompress(ciera_plan_t plan, const uint8_t *payloads_dev, int64_t payload_stride,
                      const ciera_desc *descs_dev, uint8_t *recv_cache_dev, uint16_t *out_dev,
                      void *workspace_dev, uint32_t flags, void *stream);

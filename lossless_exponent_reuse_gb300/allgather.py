@@ -22,12 +22,18 @@ class SimulatedAllgather:
     """Device state of one plan: both exponent caches, payloads, descriptors."""
 
     def __init__(self, numel: int, block: int, ranks: int, device="cuda",
-                 keep_flags: bool = False, hashed: bool = False):
+                 keep_flags: bool = False, hashed: bool = False, rans: bool = False):
+        if hashed and rans:
+            raise ValueError("the hashed change test and RANS payloads are separate senders")
         self.plan = ciera.Plan(numel, block, ranks)
         info = self.plan.info
         self.numel = numel
         self.device = torch.device(device)
         self.hashed = hashed
+        self.rans = rans
+        # RANS: each shard's exponent histogram, this call's and the previous one's
+        self.hist = ([torch.zeros((ranks, 256), dtype=torch.int32, device=device)
+                      for _ in range(2)] if rans else None)
         # the sender's state: exponents per value, or (hashed) 16 bytes per block
         self.hash_cache = (torch.zeros((ranks, max(info.blocks_per_shard, 1), 2),
                                        dtype=torch.int64, device=device) if hashed else None)
@@ -43,7 +49,12 @@ class SimulatedAllgather:
         self.iteration = 0
 
     def compress(self, w: torch.Tensor, stream=None) -> None:
-        if self.hashed:
+        if self.rans:
+            prev, cur = self.hist[self.iteration % 2], self.hist[(self.iteration + 1) % 2]
+            self.plan.compress_rans(w, self.sender_cache, prev, cur, self.payloads, self.descs,
+                                    self.workspace, cold=self.iteration == 0,
+                                    flags_out=self.flags, stream=stream)
+        elif self.hashed:
             self.plan.compress_hashed(w, self.hash_cache, self.payloads, self.descs,
                                       self.workspace, cold=self.iteration == 0,
                                       flags_out=self.flags, stream=stream)
@@ -54,7 +65,7 @@ class SimulatedAllgather:
     def decompress(self, stream=None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
         o = self.out if out is None else out
         self.plan.decompress(self.payloads, self.descs, self.recv_cache, o, self.workspace,
-                             stream=stream)
+                             rans=self.rans, stream=stream)
         self.iteration += 1
         return o
 

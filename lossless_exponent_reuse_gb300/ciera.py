@@ -30,8 +30,10 @@ E_INTERNAL = -5
 
 MODE_COMPRESSED = 0
 MODE_RAW = 1
+MODE_RANS = 2
 
 COLD = 1
+DECOMPRESS_RANS = 1
 DEBUG_SKIP_FIRST_PUBLISH = 0x80000000
 
 DESC_BYTES = 24
@@ -77,6 +79,8 @@ SIGNATURES = {
     "ciera_decompress": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _u32, _vp]),
     "ciera_compress_hashed": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _u32,
                                      _vp]),
+    "ciera_compress_rans": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp,
+                                   _u32, _vp]),
     "ciera_compress_noalloc": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _u32,
                                       _vp]),
     "ciera_pipeline_create": (_i32, [_i32, ctypes.POINTER(_vp)]),
@@ -254,9 +258,41 @@ class Plan:
             _dev_ptr(workspace, "workspace", torch.uint8), COLD if cold else 0,
             _stream_handle(stream)), "ciera_compress_hashed")
 
+    def compress_rans(self, w: torch.Tensor, sender_cache: torch.Tensor,
+                      hist_prev: torch.Tensor, hist_out: torch.Tensor, payloads: torch.Tensor,
+                      descs: torch.Tensor, workspace: torch.Tensor, *, cold: bool = False,
+                      rank_begin: int = 0, rank_count: Optional[int] = None,
+                      flags_out: Optional[torch.Tensor] = None, extra_flags: int = 0,
+                      stream=None) -> None:
+        """ciera_compress_rans: as ``compress``, with the changed exponents
+        rANS-coded.  ``hist_prev`` / ``hist_out``: rank_count x 256 int32 (the
+        exponent histogram of the previous call / of this call)."""
+        info = self.info
+        rc = info.ranks - rank_begin if rank_count is None else rank_count
+        if payloads.dim() != 2 or payloads.shape[0] < rc:
+            raise ValueError("payloads must be [rank_count, stride] uint8")
+        if descs.numel() < rc * DESC_BYTES:
+            raise ValueError("descs too small")
+        if flags_out is not None and flags_out.numel() < rc * info.blocks_per_shard:
+            raise ValueError("flags_out too small")
+        if workspace.numel() < info.workspace_bytes:
+            raise ValueError("workspace too small")
+        flags = (COLD if cold else 0) | int(extra_flags)
+        _check(lib().ciera_compress_rans(
+            self._h, int(rank_begin), int(rc),
+            _dev_ptr(w, "w", torch.uint16), _dev_ptr(sender_cache, "sender_cache", torch.uint8),
+            _dev_ptr(hist_prev, "hist_prev", torch.int32, 256 * rc),
+            _dev_ptr(hist_out, "hist_out", torch.int32, 256 * rc),
+            _dev_ptr(payloads, "payloads", torch.uint8), payloads.stride(0),
+            _dev_ptr(descs, "descs", torch.uint8), _dev_ptr(flags_out, "flags_out", torch.uint8),
+            _dev_ptr(workspace, "workspace", torch.uint8), flags, _stream_handle(stream)),
+            "ciera_compress_rans")
+
     def decompress(self, payloads: torch.Tensor, descs: torch.Tensor, recv_cache: torch.Tensor,
-                   out: torch.Tensor, workspace: torch.Tensor, *, stream=None) -> None:
-        """ciera_decompress: all R payloads -> ``out`` (uint16 bits, N values)."""
+                   out: torch.Tensor, workspace: torch.Tensor, *, rans: bool = False,
+                   stream=None) -> None:
+        """ciera_decompress: all R payloads -> ``out`` (uint16 bits, N values);
+        ``rans`` accepts RANS payloads too (CIERA_DECOMPRESS_RANS)."""
         info = self.info
         if payloads.dim() != 2 or payloads.shape[0] < info.ranks:
             raise ValueError("payloads must be [ranks, stride] uint8")
@@ -269,7 +305,8 @@ class Plan:
             _dev_ptr(descs, "descs", torch.uint8),
             _dev_ptr(recv_cache, "recv_cache", torch.uint8, info.numel),
             _dev_ptr(out, "out", torch.uint16, info.numel),
-            _dev_ptr(workspace, "workspace", torch.uint8), 0, _stream_handle(stream)),
+            _dev_ptr(workspace, "workspace", torch.uint8), DECOMPRESS_RANS if rans else 0,
+            _stream_handle(stream)),
             "ciera_decompress")
 
 

@@ -244,6 +244,58 @@ int ciera_compress_hashed(ciera_plan_t p, int rank_begin, int rank_count, const 
                        stream);
 }
 
+int ciera_compress_rans(ciera_plan_t p, int rank_begin, int rank_count, const uint16_t* w_dev,
+                        uint8_t* sender_cache_dev, const uint32_t* hist_prev_dev,
+                        uint32_t* hist_out_dev, uint8_t* payloads_dev, int64_t payload_stride,
+                        ciera_desc* descs_dev, uint8_t* flags_dev, void* workspace_dev,
+                        uint32_t flags, void* stream) {
+  if (!p || rank_begin < 0 || rank_count < 1 ||
+      static_cast<int64_t>(rank_begin) + rank_count > p->ranks)
+    return CIERA_E_INVAL;
+  if (!payloads_dev || !descs_dev || !workspace_dev || payload_stride < p->capacity ||
+      !hist_prev_dev || !hist_out_dev)
+    return CIERA_E_INVAL;
+  const uint32_t known = CIERA_COLD | CIERA_DEBUG_SKIP_FIRST_PUBLISH;
+  if (flags & ~known) return CIERA_E_INVAL;
+  // staged kernel only: every shard a multiple of 16 values, aligned operands
+  if (!p->fast || p->numel % 16 != 0 || p->S > (int64_t(1) << 30) || p->T > 32)
+    return CIERA_E_INVAL;
+  const Geometry g = range_geometry(p, rank_begin, rank_count);
+  if (g.total_tiles > 0 && (!w_dev || !sender_cache_dev)) return CIERA_E_INVAL;
+  if ((g.total_tiles > 0 && (!aligned16(w_dev) || !aligned16(sender_cache_dev))) ||
+      !aligned16(payloads_dev) || payload_stride % 16 != 0 ||
+      (reinterpret_cast<uintptr_t>(hist_prev_dev) & 3u) ||
+      (reinterpret_cast<uintptr_t>(hist_out_dev) & 3u))
+    return CIERA_E_INVAL;
+  const size_t hist_bytes = sizeof(uint32_t) * 256 * static_cast<size_t>(rank_count);
+  {
+    // the histograms must not overlap: the kernel reads one while adding into the other
+    const uintptr_t a = reinterpret_cast<uintptr_t>(hist_prev_dev);
+    const uintptr_t b = reinterpret_cast<uintptr_t>(hist_out_dev);
+    if (a < b + hist_bytes && b < a + hist_bytes) return CIERA_E_INVAL;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(hist_out_dev, 0, hist_bytes, s) != cudaSuccess) return CIERA_E_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace_dev);
+  CompressParams kp{};
+  kp.geo = g;
+  kp.w = w_dev;
+  kp.scache = sender_cache_dev;
+  kp.payloads = payloads_dev;
+  kp.stride = payload_stride;
+  kp.descs = descs_dev;
+  kp.flagbytes = flags_dev ? flags_dev : ws + p->off_flags;
+  kp.flag_stride = flags_dev ? p->nb_full : p->flag_stride;
+  kp.tile_status = reinterpret_cast<unsigned long long*>(ws + p->off_status);
+  kp.tile_flags = reinterpret_cast<unsigned long long*>(ws + p->off_tflags);
+  kp.ctl = reinterpret_cast<Control*>(ws);
+  kp.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  kp.flags = flags;
+  kp.fast = 1;
+  const int e = launch_compress_rans(kp, hist_prev_dev, hist_out_dev, stream);
+  return e == cudaSuccess ? CIERA_OK : CIERA_E_CUDA;
+}
+
 }  // extern "C"
 
 struct ciera_pipeline_s {
@@ -312,7 +364,7 @@ int ciera_decompress(ciera_plan_t p, const uint8_t* payloads_dev, int64_t payloa
                      const ciera_desc* descs_dev, uint8_t* recv_cache_dev, uint16_t* out_dev,
                      void* workspace_dev, uint32_t flags, void* stream) {
   if (!p || !payloads_dev || !descs_dev || !workspace_dev || payload_stride < p->capacity ||
-      flags != 0)
+      (flags & ~CIERA_DECOMPRESS_RANS))
     return CIERA_E_INVAL;
   if (p->numel > 0 && (!recv_cache_dev || !out_dev)) return CIERA_E_INVAL;
   uint8_t* ws = static_cast<uint8_t*>(workspace_dev);
@@ -331,7 +383,12 @@ int ciera_decompress(ciera_plan_t p, const uint8_t* payloads_dev, int64_t payloa
   kp.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   kp.fast = p->fast && aligned16(payloads_dev) && (payload_stride % 16 == 0) &&
             aligned16(recv_cache_dev) && aligned16(out_dev);
-  const int e = launch_decompress(kp, kp.fast ? p->smem_decompress : 0, stream);
+  if (flags & CIERA_DECOMPRESS_RANS) {
+    if (!kp.fast || p->numel % 16 != 0) return CIERA_E_INVAL;
+    kp.rans = 1;
+  }
+  int e = launch_decompress(kp, kp.fast ? p->smem_decompress : 0, stream);
+  if (e == cudaSuccess && kp.rans) e = launch_decompress_rans(kp, stream);
   return e == cudaSuccess ? CIERA_OK : CIERA_E_CUDA;
 }
 

@@ -711,9 +711,10 @@ int oracle_rans_decode_block(const uint8_t *rec, int64_t rec_bytes, int64_t L,
  *   [0, len)             sign+mantissa byte of every value
  *   A = align16(len)     bitmap, ceil(n_b/8) bytes
  *   C = align16(A + bm)  frequency table, 256 uint16
- *   O = C + 512          record offset of every block, uint32 (relative to D;
- *                        0 for an unchanged block)
- *   D = align16(O + 4 n_b)  the records of the changed blocks, in order
+ *   O = C + 512          n_b + 1 uint32: entry k = bytes of the records of
+ *                        blocks before k (record k spans entries k .. k+1,
+ *                        empty for an unchanged block); entry n_b = total
+ *   D = align16(O + 4 (n_b + 1))  the records of the changed blocks, in order
  * Descriptor: mode 2, body_bytes = D, payload_bytes = D + records.  RAW as
  * before when cold, empty, or when the payload would not be smaller than
  * 2*len.  hist_prev: histogram of the shard's exponents one iteration
@@ -728,7 +729,7 @@ int oracle_compress_shard_rans(const uint16_t *shard, int64_t len, int64_t block
     int64_t A = (len + 15) / 16 * 16;
     int64_t C = (A + bm + 15) / 16 * 16;
     int64_t O = C + 512;
-    int64_t D = (O + 4 * nblocks + 15) / 16 * 16;
+    int64_t D = (O + 4 * (nblocks + 1) + 15) / 16 * 16;
     int64_t pos = 0, k, j;
     uint16_t freq[256];
     uint8_t *exps = (uint8_t *)malloc((size_t)(block > 0 ? block : 1));
@@ -774,11 +775,14 @@ int oracle_compress_shard_rans(const uint16_t *shard, int64_t len, int64_t block
             tmp[C + 2 * j + 1] = (uint8_t)(freq[j] >> 8);
         }
         pos = D;
-        for (k = 0; k < nblocks; ++k) {
+        for (k = 0; k <= nblocks; ++k) {
             int64_t lo = k * block;
             int64_t hi = lo + block < len ? lo + block : len;
             int64_t size;
-            if (!flags_out[k]) {
+            for (j = 0; j < 4; ++j) {
+                tmp[O + 4 * k + j] = (uint8_t)(((uint64_t)(pos - D) >> (8 * j)) & 0xFF);
+            }
+            if (k == nblocks || !flags_out[k]) {
                 continue;
             }
             ++n_changed;
@@ -789,9 +793,6 @@ int oracle_compress_shard_rans(const uint16_t *shard, int64_t len, int64_t block
             if (pos + size >= 2 * len) {
                 raw = 1;
                 break;
-            }
-            for (j = 0; j < 4; ++j) {
-                tmp[O + 4 * k + j] = (uint8_t)(((uint64_t)(pos - D) >> (8 * j)) & 0xFF);
             }
             memcpy(tmp + pos, rec, (size_t)size);
             pos += size;
@@ -843,7 +844,7 @@ int oracle_decompress_shard_rans(const uint8_t *payload, const oracle_desc *d, i
     int64_t A = (len + 15) / 16 * 16;
     int64_t C = (A + bm + 15) / 16 * 16;
     int64_t O = C + 512;
-    int64_t D = (O + 4 * nblocks + 15) / 16 * 16;
+    int64_t D = (O + 4 * (nblocks + 1) + 15) / 16 * 16;
     int64_t k, j;
     uint16_t freq[256];
     uint32_t sum = 0, seen = 0;
@@ -869,14 +870,15 @@ int oracle_decompress_shard_rans(const uint8_t *payload, const oracle_desc *d, i
         int64_t hi = lo + block < len ? lo + block : len;
         int changed = (payload[A + k / 8] >> (k % 8)) & 1;
         if (changed) {
-            uint64_t off = 0;
+            uint64_t off = 0, end = 0;
             ++seen;
             for (j = 0; j < 4; ++j) {
                 off |= (uint64_t)payload[O + 4 * k + j] << (8 * j);
+                end |= (uint64_t)payload[O + 4 * (k + 1) + j] << (8 * j);
             }
-            if (D + off >= d->payload_bytes ||
-                oracle_rans_decode_block(payload + D + off, (int64_t)(d->payload_bytes - D - off),
-                                         hi - lo, freq, exps) != 0) {
+            if (end <= off || D + end > d->payload_bytes ||
+                oracle_rans_decode_block(payload + D + off, (int64_t)(end - off), hi - lo, freq,
+                                         exps) != 0) {
                 free(exps);
                 return -1;
             }

@@ -86,8 +86,8 @@ def test_compress_rejects_bad_ranges_without_touching_the_gpu():
                             None) == ciera.E_INVAL                  # unknown flag
     assert L.ciera_decompress(p.handle, fake, cap - 1, fake, fake, fake, fake, 0,
                               None) == ciera.E_INVAL
-    assert L.ciera_decompress(p.handle, fake, cap, fake, fake, fake, fake, 1,
-                              None) == ciera.E_INVAL
+    assert L.ciera_decompress(p.handle, fake, cap, fake, fake, fake, fake, 2,
+                              None) == ciera.E_INVAL                # unknown flag
 
 
 def test_predicate_matches_oracle():
@@ -136,3 +136,33 @@ def test_hashed_compress_needs_tiles_of_at_most_32_blocks():
     fake = ctypes.c_void_p(4096)              # never dereferenced: the check fails first
     assert L.ciera_compress_hashed(p.handle, 0, 4, fake, fake, fake, cap, fake, None, fake, 0,
                                    None) == ciera.E_INVAL
+
+
+def test_rans_entry_points_reject_what_the_staged_kernels_cannot_take():
+    L = ciera.lib()
+    fake = ctypes.c_void_p(4096)              # never dereferenced: the checks fail first
+    odd = ctypes.c_void_p(4097)
+
+    def rans(plan, w=fake, hp=fake, ho=ctypes.c_void_p(1 << 20), stride=None, flags=0):
+        cap = plan.info.payload_capacity if stride is None else stride
+        return L.ciera_compress_rans(plan.handle, 0, plan.info.ranks, w, fake, hp, ho, fake,
+                                     cap, fake, None, fake, flags, None)
+
+    assert rans(ciera.Plan(100003, 256, 3)) == ciera.E_INVAL    # no staged path (S % 16)
+    assert rans(ciera.Plan(131069, 256, 4)) == ciera.E_INVAL    # N % 16 != 0
+    assert rans(ciera.Plan(65536, 128, 2)) == ciera.E_INVAL     # block below 256
+    p = ciera.Plan(131072, 256, 4)
+    assert rans(p, w=odd) == ciera.E_INVAL                      # unaligned values
+    assert rans(p, hp=ctypes.c_void_p(4098)) == ciera.E_INVAL   # unaligned histogram
+    assert rans(p, ho=ctypes.c_void_p(4096 + 1024)) == ciera.E_INVAL  # histograms overlap
+    assert rans(p, stride=p.info.payload_capacity + 8) == ciera.E_INVAL  # stride % 16
+    assert rans(p, flags=0x40) == ciera.E_INVAL
+    assert L.ciera_compress_rans(p.handle, 0, 4, fake, fake, None, fake, fake,
+                                 p.info.payload_capacity, fake, None, fake, 0,
+                                 None) == ciera.E_INVAL        # no histogram
+    # the receiver takes RANS payloads only on the staged path
+    q = ciera.Plan(100003, 256, 3)
+    assert L.ciera_decompress(q.handle, fake, q.info.payload_capacity, fake, fake, fake, fake,
+                              ciera.DECOMPRESS_RANS, None) == ciera.E_INVAL
+    assert L.ciera_decompress(p.handle, fake, p.info.payload_capacity, fake, odd, fake, fake,
+                              ciera.DECOMPRESS_RANS, None) == ciera.E_INVAL
