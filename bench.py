@@ -57,7 +57,7 @@ def parse_args():
                     help="sequential: compress then decompress layer by layer (per-kernel "
                          "timing); pipelined: compress(i+1) on a side stream overlapping "
                          "decompress(i); graph: the pipelined step replayed from a CUDA graph")
-    ap.add_argument("--sender", choices=["exact", "hash"], default="exact",
+    ap.add_argument("--sender", choices=["exact", "hash", "rans"], default="exact",
                     help="change test: exact exponent compare (default) or the 128-bit "
                          "block hash with a 16-byte-per-block HashCache")
     ap.add_argument("--no-e2e", action="store_true")
@@ -157,13 +157,24 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------
 
+def kernel_source_hash(kernel):
+    """sha256 prefix of the sources `kernel` is compiled from (its .cu file,
+    the shared device helpers and the launch parameters)."""
+    import hashlib
+    csrc = os.path.join(ROOT, "lossless_exponent_reuse_gb300", "csrc")
+    rans = kernel.endswith("_rans")
+    units = ("ciera_rans.cu", "ciera_rans.h") if rans else ("ciera_kernels.cu",)
+    h = hashlib.sha256()
+    for name in units + ("ciera_device.cuh", "ciera_internal.h"):
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def traffic_per_value(kernel):
     """DRAM bytes per value of `kernel` from profiles/traffic.md, or None if
     that capture was taken on a different kernel source."""
-    import hashlib
-    src = os.path.join(ROOT, "lossless_exponent_reuse_gb300", "csrc", "ciera_kernels.cu")
     try:
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        h = kernel_source_hash(kernel)
         for line in open(os.path.join(ROOT, "profiles", "traffic.md")):
             cells = [c.strip() for c in line.strip().strip("|").split("|")]
             if len(cells) >= 3 and cells[0] == kernel and cells[1] == h:
@@ -190,18 +201,22 @@ def algorithmic_bytes(descs, numel, hashed=False, block=4096):
     decompress: read payloads P + cached exponents of kept values N - C,
                 write out 2N + exponents of changed values C = 3N + P
     A raw payload counts all its values as changed; a compressed body holds
-    len + (values in changed blocks) bytes.
+    len + (values in changed blocks) bytes; a RANS payload's changed values
+    are those of its changed blocks.
     """
+    R = len(descs)
+    S = -(-numel // R)
+    lens = [max(0, min(S, numel - r * S)) for r in range(R)]
     P = sum(d["payload_bytes"] for d in descs)
     raw_vals = sum(d["payload_bytes"] // 2 for d in descs if d["mode"] == 1)
-    comp_vals = numel - raw_vals
+    comp_vals = sum(ln for d, ln in zip(descs, lens) if d["mode"] == 0)
     comp_changed = sum(d["body_bytes"] for d in descs if d["mode"] == 0) - comp_vals
-    C = raw_vals + comp_changed
+    rans_changed = sum(min(d["n_changed_blocks"] * block, ln)
+                       for d, ln in zip(descs, lens) if d["mode"] == 2)
+    C = raw_vals + comp_changed + rans_changed
     if hashed:
         # hashed sender: reads w 2N + 16 B of HashCache per block, writes
         # payloads P + 16 B per changed block
-        R = len(descs)
-        S = -(-numel // R)
         blocks = sum(-(-max(0, min(S, numel - r * S)) // block) for r in range(R))
         changed = sum(d["n_changed_blocks"] for d in descs)
         return 2 * numel + 16 * blocks + P + 16 * changed, 3 * numel + P, C / max(numel, 1)
@@ -300,7 +315,8 @@ def run_ours(args, world, rank, local):
     L = wl.layers
     gen = iteration_buckets(wl, W + K, dev)
     hashed = args.sender == "hash"
-    layers = [SimulatedAllgather(n, wl.block, wl.ranks, device=dev, hashed=hashed)
+    rans = args.sender == "rans"
+    layers = [SimulatedAllgather(n, wl.block, wl.ranks, device=dev, hashed=hashed, rans=rans)
               for _ in range(L)]
     stream = torch.cuda.current_stream()
     warm_host = []                                  # iterations W-1, W of layer 0 for the oracle
@@ -316,7 +332,8 @@ def run_ours(args, world, rank, local):
     seq = [next(gen) for _ in range(K)]             # timed inputs, resident in HBM
     warm_host.append(seq[0][0].view(torch.int16).cpu().numpy().view(np.uint16))
     del gen
-    snaps = [(ag.hash_cache.clone() if hashed else ag.sender_cache.clone(), ag.recv_cache.clone())
+    snaps = [(ag.hash_cache.clone() if hashed else ag.sender_cache.clone(), ag.recv_cache.clone(),
+              [h.clone() for h in ag.hist] if rans else None)
              for ag in layers]
     it0 = layers[0].iteration
     torch.cuda.synchronize()
@@ -330,7 +347,7 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     sched = args.schedule
-    if sched != "sequential" and hashed:
+    if sched != "sequential" and (hashed or rans):
         raise SystemExit("the pipelined schedules drive the exact sender")
     pipe = ciera.Pipeline(L) if sched != "sequential" else None
     graphs = []
@@ -384,9 +401,12 @@ def run_ours(args, world, rank, local):
 
     # untimed replay from the same state: per-step descriptors for the byte
     # accounting, and a determinism check against the timed run
-    for ag, (sc, rc) in zip(layers, snaps):
+    for ag, (sc, rc, hs) in zip(layers, snaps):
         (ag.hash_cache if hashed else ag.sender_cache).copy_(sc)
         ag.recv_cache.copy_(rc)
+        if rans:
+            for h, h0 in zip(ag.hist, hs):
+                h.copy_(h0)
         ag.iteration = it0
     del snaps
     bytes_c, bytes_d, fvals = [], [], []
@@ -442,8 +462,13 @@ def run_ours(args, world, rank, local):
         dom_bytes = statistics.mean([c_ + d_ for c_, d_ in zip(bytes_c, bytes_d)])
         dom_ms = statistics.mean(step_ms)
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-    tpv = (traffic_per_value(("k_compress_hashed" if hashed else "k_compress")
-                             if dom == "k_compress" else "k_decompress")
+    kname = "k_compress_hashed" if hashed else ("k_compress_rans" if rans else "k_compress")
+    if dom == "k_compress":
+        dom = kname
+    elif rans and t_c is not None:
+        dom += "+k_decompress_rans"
+    tpv = (traffic_per_value(kname if dom == kname else
+                             ("k_decompress_rans" if rans else "k_decompress"))
            if t_c is not None else None)
     traffic = round(tpv * n) if tpv is not None else None
     cfg = {"workload": wl.name, "sender": args.sender, "schedule": sched, "numel": n * L,
@@ -468,7 +493,8 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "peak_kind": peak_kind},
-        "gpu_launches": K * L * 3,
+        # compress (+ the RANS raw fixup), bitmap scan, decompress (+ the RANS tiles)
+        "gpu_launches": K * L * (5 if rans else 3),
         "clocks": clk,
     }
 
@@ -476,7 +502,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.empty_cache()
     if not args.no_e2e:
         if L == 1:
-            result["e2e"] = run_e2e(wl, [s_[0] for s_ in seq], n, K, dev, world, hashed)
+            result["e2e"] = run_e2e(wl, [s_[0] for s_ in seq], n, K, dev, world, hashed, rans)
         else:
             result["e2e"] = None
     del seq
@@ -485,7 +511,7 @@ def run_ours(args, world, rank, local):
     return result
 
 
-def run_e2e(wl, seq, n, K, dev, world, hashed=False):
+def run_e2e(wl, seq, n, K, dev, world, hashed=False, rans=False):
     """The same metric through host buffers: each step copies its weights
     from pinned host memory, runs the path and copies the rebuilt weights
     back, with neighbouring steps' uploads and downloads overlapped
@@ -495,7 +521,7 @@ def run_e2e(wl, seq, n, K, dev, world, hashed=False):
     from lossless_exponent_reuse_gb300.allgather import HostStreamer, SimulatedAllgather
     host = [s.view(torch.int16).to("cpu").pin_memory() for s in seq]
     outs = [torch.empty(n, dtype=torch.int16).pin_memory() for _ in range(2)]
-    ag = SimulatedAllgather(n, wl.block, wl.ranks, device=dev, hashed=hashed)
+    ag = SimulatedAllgather(n, wl.block, wl.ranks, device=dev, hashed=hashed, rans=rans)
     hs = HostStreamer(ag)
     stream = torch.cuda.current_stream()
     for t in range(min(3, len(host))):               # warm-up (first call is the cold start)

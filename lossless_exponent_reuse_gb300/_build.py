@@ -12,7 +12,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libciera.so")
 SOURCES = ["ciera_kernels.cu", "ciera_rans.cu", "ciera_api.cpp", "ciera_noalloc.cu"]
 HEADERS = [os.path.join(ROOT, "include", "ciera.h"), os.path.join(CSRC, "ciera_internal.h"),
-           os.path.join(CSRC, "ciera_device.cuh")]
+           os.path.join(CSRC, "ciera_device.cuh"), os.path.join(CSRC, "ciera_rans.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

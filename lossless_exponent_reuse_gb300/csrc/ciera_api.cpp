@@ -16,6 +16,7 @@
 
 #include "ciera.h"
 #include "ciera_internal.h"
+#include "ciera_rans.h"
 
 using namespace ciera;
 

@@ -38,6 +38,7 @@
 
 #include "ciera_device.cuh"
 #include "ciera_internal.h"
+#include "ciera_rans.h"
 
 namespace ciera {
 namespace {
