@@ -35,7 +35,9 @@ struct ciera_plan_s {
   int64_t capacity;
   int64_t flag_stride;
   int64_t nw_stride;
-  int64_t off_status, off_tflags, off_flags, off_words, off_prefix, off_rstate, ws_bytes;
+  int64_t off_status, off_tflags, off_flags, off_words, off_prefix, off_rstate;
+  int64_t off_renc, off_rdec;  // per-rank RANS coder tables (encoder, decoder)
+  int64_t ws_bytes;
   int64_t smem_flags;         // flag words of every compress call (exact test)
   int64_t smem_flags_hashed;  // ... plus the per-block hash sums (hashed test)
   int64_t smem_decompress;
@@ -135,7 +137,9 @@ int ciera_plan(const int64_t* shape, int ndim, int64_t block, int ranks, ciera_p
   p->off_words = align_up(p->off_flags + p->flag_stride * ranks, 256);
   p->off_prefix = align_up(p->off_words + 4 * p->nw_stride * ranks, 256);
   p->off_rstate = align_up(p->off_prefix + 4 * p->nw_stride * ranks, 256);
-  p->ws_bytes = align_up(p->off_rstate + 4 * static_cast<int64_t>(ranks), 256);
+  p->off_renc = align_up(p->off_rstate + 4 * static_cast<int64_t>(ranks), 256);
+  p->off_rdec = align_up(p->off_renc + kRansEncTableBytes * ranks, 256);
+  p->ws_bytes = align_up(p->off_rdec + kRansDecTableBytes * ranks, 256);
   p->fast = (block % 16 == 0) && block >= kFastMinBlock && block <= kFastMaxBlock &&
             (p->S % 16 == 0);
   // compress: flag words + their prefix (every call), then 2*TE values and
@@ -293,7 +297,7 @@ int ciera_compress_rans(ciera_plan_t p, int rank_begin, int rank_count, const ui
   kp.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   kp.flags = flags;
   kp.fast = 1;
-  const int e = launch_compress_rans(kp, hist_prev_dev, hist_out_dev, stream);
+  const int e = launch_compress_rans(kp, hist_prev_dev, hist_out_dev, ws + p->off_renc, stream);
   return e == cudaSuccess ? CIERA_OK : CIERA_E_CUDA;
 }
 
@@ -389,7 +393,8 @@ int ciera_decompress(ciera_plan_t p, const uint8_t* payloads_dev, int64_t payloa
     kp.rans = 1;
   }
   int e = launch_decompress(kp, kp.fast ? p->smem_decompress : 0, stream);
-  if (e == cudaSuccess && kp.rans) e = launch_decompress_rans(kp, stream);
+  if (e == cudaSuccess && kp.rans)
+    e = launch_decompress_rans(kp, reinterpret_cast<uint32_t*>(ws + p->off_rdec), stream);
   return e == cudaSuccess ? CIERA_OK : CIERA_E_CUDA;
 }
 

@@ -21,6 +21,11 @@
 // iteration earlier, which the previous call accumulated as a by-product.
 //
 // Kernels:
+//   k_rans_enc_tables  one CTA per rank: frequencies from the histogram, and
+//                      per symbol the constants of an exact division by its
+//                      frequency (Granlund and Montgomery, "Division by
+//                      invariant integers using multiplication", 1994), so
+//                      that a coding step multiplies instead of dividing.
 //   k_compress_rans    one CTA per tile, ticket order: flags (exact test)
 //                      and the exponent histogram, cache refresh, sign+
 //                      mantissa bytes to their fixed positions, one warp
@@ -28,10 +33,13 @@
 //                      the record sizes places the records.
 //   k_rans_raw_fixup   rewrites a shard raw when its RANS payload would not
 //                      have been smaller than the raw bytes.
+//   k_rans_dec_tables  one CTA per RANS rank: a slot -> (symbol, frequency,
+//                      bias) table of 4096 entries from the received
+//                      frequencies, so that a decoding step is one lookup.
 //   k_decompress_rans  one CTA per tile of a RANS rank: bulk copies of the
-//                      sign+mantissa bytes, cached exponents, table and
-//                      records; one warp per changed block decodes it; merge;
-//                      ExpCache refresh.
+//                      sign+mantissa bytes, cached exponents, slot table and
+//                      records; one warp per changed block decodes it; merge
+//                      straight to the output; ExpCache refresh.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -46,38 +54,53 @@ namespace {
 constexpr int kRansBits = 12;
 constexpr uint32_t kRansTotal = 1u << kRansBits;
 constexpr uint32_t kRansLow = 1u << 16;
+constexpr int kTableThreads = 256;
 
-// ---- meta region offsets (bytes) inside the first kRansMetaBytes ----------
-// compress
-constexpr int kCFw = 0;          // uint32 flag bits of the tile (T <= 32)
-constexpr int kCFreq = 16;       // uint16[256]
-constexpr int kCCum = 544;       // uint32[257]
-constexpr int kCHist = 1584;     // uint32[256] exponent histogram of the tile
-constexpr int kCSize = 2624;     // uint32[32] record size of each block, 16-byte units
-constexpr int kCPre = 2752;      // uint32[33] exclusive prefix of the sizes
-constexpr int kCRed = 2896;      // uint64[8] reductions
-// decompress
-constexpr int kDFreq = 0;        // uint16[256], bulk-copied from the payload
-constexpr int kDCum = 512;       // uint32[257]
-constexpr int kDOffs = 1552;     // uint32[33] record-byte prefixes of the tile's blocks
-constexpr int kDRed = 1696;      // uint64[8]
-constexpr int kDSlot = 2048;     // uint8[4096] slot -> symbol
-static_assert(kDSlot + 4096 <= kRansMetaBytes, "meta region");
-static_assert(kCRed + 64 <= kRansMetaBytes, "meta region");
+// ---- shared-memory meta region of k_compress_rans (bytes) ----------------
+constexpr int kCTab = 0;         // uint64[256] coder entries, then uint16[256] frequencies
+constexpr int kCFreq = 2048;
+constexpr int kCHist = 2560;     // uint32[256] exponent histogram of the tile
+constexpr int kCSize = 3584;     // uint32[32] record size of each block, 16-byte units
+constexpr int kCPre = 3712;      // uint32[33] exclusive prefix of the sizes
+constexpr int kCRed = 3856;      // uint32[8] reductions
+constexpr int kCFw = 3920;       // uint32 flag bits of the tile (T <= 32)
+static_assert(kCFw + 4 <= kRansEncMeta, "meta region");
+static_assert(kCFreq - kCTab + 512 == kRansEncTableBytes, "coder table layout");
+// ---- k_decompress_rans ---------------------------------------------------
+constexpr int kDOffs = 0;        // uint32[33] record-byte prefixes of the tile's blocks
+static_assert(kDOffs + 4 * 33 <= kRansDecMeta, "meta region");
 
-// Block-wide sum over all 128 threads (uses red[0..3]; ends with a barrier).
-__device__ __forceinline__ unsigned long long block_sum(unsigned long long v,
+// Coder entry of a symbol of frequency f and cumulative frequency c:
+//   bits  0..31  m, the multiplier of floor(x / f) = (t + ((x - t) >> s1)) >> s2,
+//                t = mulhi(x, m), l = ceil(log2 f), m = floor(2^32 (2^l - f) / f) + 1,
+//                s1 = min(l, 1), s2 = max(l - 1, 0)
+//   bits 32..43  c
+//   bits 44..55  4096 - f
+//   bits 56..59  s2,  bit 60  s1
+__device__ __forceinline__ unsigned long long coder_entry(uint32_t f, uint32_t c) {
+  const uint32_t l = 32u - __clz(f - 1u);  // ceil(log2 f); 0 for f = 1
+  const unsigned long long num = (1ull << 32) * ((1ull << l) - f);
+  const uint32_t m = static_cast<uint32_t>(num / f + 1ull);
+  const uint32_t s1 = l < 1u ? l : 1u;
+  const uint32_t s2 = l > 1u ? l - 1u : 0u;
+  const uint32_t hi = c | ((kRansTotal - f) << 12) | (s2 << 24) | (s1 << 28);
+  return (static_cast<unsigned long long>(hi) << 32) | m;
+}
+
+// Block-wide reductions over the 256 threads of a table kernel.
+__device__ __forceinline__ unsigned long long table_sum(unsigned long long v,
                                                         unsigned long long* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
-  const unsigned long long t = red[0] + red[1] + red[2] + red[3];
+  unsigned long long t = 0;
+  for (int i = 0; i < kTableThreads / 32; ++i) t += red[i];
   __syncthreads();
   return t;
 }
 
-__device__ __forceinline__ unsigned long long block_max(unsigned long long v,
+__device__ __forceinline__ unsigned long long table_max(unsigned long long v,
                                                         unsigned long long* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -86,14 +109,14 @@ __device__ __forceinline__ unsigned long long block_max(unsigned long long v,
   }
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
-  unsigned long long t = red[0];
-  for (int i = 1; i < 4; ++i) t = red[i] > t ? red[i] : t;
+  unsigned long long t = 0;
+  for (int i = 0; i < kTableThreads / 32; ++i) t = red[i] > t ? red[i] : t;
   __syncthreads();
   return t;
 }
 
-// Exclusive scan of `v` over the 128 threads (uses red[4..7]).
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, unsigned long long* red) {
+// Exclusive prefix sum over the 256 threads.
+__device__ __forceinline__ uint32_t table_exclusive_scan(uint32_t v, unsigned long long* red) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   uint32_t incl = v;
 #pragma unroll
@@ -101,63 +124,72 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, unsigned lo
     const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += u;
   }
-  if (lane == 31) red[4 + wid] = incl;
+  if (lane == 31) red[wid] = incl;
   __syncthreads();
   uint32_t base = 0;
-  for (int i = 0; i < wid; ++i) base += static_cast<uint32_t>(red[4 + i]);
+  for (int i = 0; i < wid; ++i) base += static_cast<uint32_t>(red[i]);
   __syncthreads();
   return base + incl - v;
 }
 
-// Frequency table from a histogram (all 128 threads; symbols 2t, 2t+1 per
-// thread): f = 1 + floor(h * 3840 / sum h), the rest of 4096 to the most
-// frequent symbol (lowest on a tie), 16 each for an empty histogram.
-__device__ void build_table(const uint32_t* h, uint16_t* freq, uint32_t* cum,
-                            unsigned long long* red) {
-  const int t = threadIdx.x;
-  const uint32_t h0 = h[2 * t], h1 = h[2 * t + 1];
-  const unsigned long long total = block_sum(static_cast<unsigned long long>(h0) + h1, red);
-  uint32_t f0 = 16, f1 = 16;
+// One CTA per rank of the range: the shard's frequencies from its exponent
+// histogram one iteration earlier, f = 1 + floor(h * 3840 / sum h), the rest
+// of 4096 to the most frequent symbol (lowest on a tie), 16 each for an
+// empty histogram; then the coder entries.
+__global__ void __launch_bounds__(kTableThreads)
+    k_rans_enc_tables(const uint32_t* __restrict__ hist_prev, uint8_t* __restrict__ tables) {
+  __shared__ unsigned long long red[kTableThreads / 32];
+  const int s = threadIdx.x;
+  const uint32_t h = hist_prev[256 * static_cast<int64_t>(blockIdx.x) + s];
+  const unsigned long long total = table_sum(h, red);
+  uint32_t f = 16;
   if (total) {
-    f0 = 1u + static_cast<uint32_t>(static_cast<unsigned long long>(h0) * 3840ull / total);
-    f1 = 1u + static_cast<uint32_t>(static_cast<unsigned long long>(h1) * 3840ull / total);
-    const unsigned long long sum = block_sum(f0 + f1, red);
-    // largest count, lowest symbol on a tie
-    const unsigned long long k0 = (static_cast<unsigned long long>(h0) << 8) | (255u - 2 * t);
-    const unsigned long long k1 = (static_cast<unsigned long long>(h1) << 8) | (254u - 2 * t);
-    const unsigned long long best = block_max(k0 > k1 ? k0 : k1, red);
-    const uint32_t bs = 255u - static_cast<uint32_t>(best & 255u);
-    const uint32_t rem = kRansTotal - static_cast<uint32_t>(sum);
-    if (bs == 2u * t) f0 += rem;
-    if (bs == 2u * t + 1) f1 += rem;
+    f = 1u + static_cast<uint32_t>(static_cast<unsigned long long>(h) * 3840ull / total);
+    const unsigned long long sum = table_sum(f, red);
+    const unsigned long long best =
+        table_max((static_cast<unsigned long long>(h) << 8) | (255u - s), red);
+    if (255u - static_cast<uint32_t>(best & 255u) == static_cast<uint32_t>(s))
+      f += kRansTotal - static_cast<uint32_t>(sum);
   }
-  freq[2 * t] = static_cast<uint16_t>(f0);
-  freq[2 * t + 1] = static_cast<uint16_t>(f1);
-  const uint32_t c = block_exclusive_scan(f0 + f1, red);
-  cum[2 * t] = c;
-  cum[2 * t + 1] = c + f0;
-  if (t == 0) cum[256] = kRansTotal;
-  __syncthreads();
+  const uint32_t c = table_exclusive_scan(f, red);
+  uint8_t* t = tables + kRansEncTableBytes * static_cast<int64_t>(blockIdx.x);
+  reinterpret_cast<unsigned long long*>(t)[s] = coder_entry(f, c);
+  reinterpret_cast<uint16_t*>(t + 2048)[s] = static_cast<uint16_t>(f);
 }
 
 // One warp codes one block of L values (their exponents) into `rec`: lane
 // counts at rec[0..31], lane regions of LW words from rec[32]; then the
 // streams are compacted in place behind the counts and padded to 16 bytes.
 // Returns the record size in 16-byte units.
-__device__ uint32_t rans_encode_block(const uint16_t* vals, int64_t L, const uint16_t* freq,
-                                      const uint32_t* cum, uint16_t* rec, int64_t LW, int lane) {
+__device__ uint32_t rans_encode_block(const uint16_t* vals, int64_t L,
+                                      const unsigned long long* tab, uint16_t* rec, int64_t LW,
+                                      int lane) {
   uint16_t* region = rec + kRansLanes + lane * LW;
   int64_t top = LW;
   uint32_t x = kRansLow;
   if (lane < L) {
-    for (int64_t j = lane + ((L - 1 - lane) / kRansLanes) * kRansLanes; j >= 0; j -= kRansLanes) {
-      const uint32_t sym = exp1(vals[j]);
-      const uint32_t f = freq[sym];
-      if (static_cast<unsigned long long>(x) >= (static_cast<unsigned long long>(f) << 20)) {
+    int64_t j = lane + ((L - 1 - lane) / kRansLanes) * kRansLanes;
+    unsigned long long E = tab[exp1(vals[j])];
+    for (;;) {
+      // the next symbol's entry is loaded while this one is coded
+      const int64_t jn = j - kRansLanes;
+      const unsigned long long En = jn >= 0 ? tab[exp1(vals[jn])] : 0ull;
+      const uint32_t m = static_cast<uint32_t>(E);
+      const uint32_t hi = static_cast<uint32_t>(E >> 32);
+      const uint32_t c = hi & 0xFFFu;
+      const uint32_t cm = (hi >> 12) & 0xFFFu;
+      const uint32_t s2 = (hi >> 24) & 0xFu;
+      const uint32_t s1 = hi >> 28;
+      if (x >= ((kRansTotal - cm) << 20)) {  // x >= f * 2^20: emit the low 16 bits
         region[--top] = static_cast<uint16_t>(x & 0xFFFFu);
         x >>= 16;
       }
-      x = ((x / f) << kRansBits) + (x % f) + cum[sym];
+      const uint32_t t = __umulhi(x, m);
+      const uint32_t q = (t + ((x - t) >> s1)) >> s2;  // floor(x / f)
+      x += q * cm + c;                                 // (q << 12) + x - q f + c
+      if (jn < 0) break;
+      j = jn;
+      E = En;
     }
   }
   region[--top] = static_cast<uint16_t>(x & 0xFFFFu);
@@ -196,11 +228,11 @@ __device__ uint32_t rans_encode_block(const uint16_t* vals, int64_t L, const uin
   return padded / 8u;
 }
 
-// One warp decodes one record of `rec_words` words into L exponents.
-// False (for the whole warp) if the record does not decode cleanly.
+// One warp decodes one record of `rec_words` words into L exponents with the
+// slot table `tab` (entry: symbol | f << 8 | (slot - cum) << 20).  False
+// (for the whole warp) if the record does not decode cleanly.
 __device__ bool rans_decode_block(const uint16_t* rec, uint32_t rec_words, int64_t L,
-                                  const uint16_t* freq, const uint32_t* cum,
-                                  const uint8_t* slot_sym, uint8_t* exps, int lane) {
+                                  const uint32_t* tab, uint8_t* exps, int lane) {
   const uint32_t nw = rec_words >= kRansLanes ? rec[lane] : 0u;
   uint32_t incl = nw;
 #pragma unroll
@@ -215,17 +247,19 @@ __device__ bool rans_decode_block(const uint16_t* rec, uint32_t rec_words, int64
   const uint16_t* s = rec + kRansLanes + pre;
   uint32_t x = (static_cast<uint32_t>(s[0]) << 16) | s[1];
   uint32_t idx = 2;
+  uint32_t nxt = idx < nw ? s[idx] : 0u;  // the next renormalisation word, loaded ahead
   for (int64_t j = lane; j < L; j += kRansLanes) {
-    const uint32_t slot = x & (kRansTotal - 1);
-    const uint32_t sym = slot_sym[slot];
-    exps[j] = static_cast<uint8_t>(sym);
-    x = static_cast<uint32_t>(freq[sym]) * (x >> kRansBits) + slot - cum[sym];
+    const uint32_t e = tab[x & (kRansTotal - 1)];
+    exps[j] = static_cast<uint8_t>(e);
+    x = ((e >> 8) & 0xFFFu) * (x >> kRansBits) + (e >> 20);
     if (x < kRansLow) {
       if (idx >= nw) {
         bad = true;
         break;
       }
-      x = (x << 16) | s[idx++];
+      x = (x << 16) | nxt;
+      ++idx;
+      nxt = idx < nw ? s[idx] : 0u;
     }
   }
   bad = bad || idx != nw || x != kRansLow;
@@ -241,7 +275,7 @@ struct RansShared {
 };
 
 __global__ void __launch_bounds__(kThreads)
-    k_compress_rans(const CompressParams p, const uint32_t* __restrict__ hist_prev,
+    k_compress_rans(const CompressParams p, const uint8_t* __restrict__ enc_tables,
                     uint32_t* __restrict__ hist_out) {
   extern __shared__ __align__(128) uint8_t dsm[];
   __shared__ RansShared sh;
@@ -251,16 +285,16 @@ __global__ void __launch_bounds__(kThreads)
   const int64_t B = p.geo.B;
   const int64_t T = p.geo.T;
   const int64_t TE = T * B;
-  uint32_t* fw = reinterpret_cast<uint32_t*>(dsm + kCFw);
-  uint16_t* freq = reinterpret_cast<uint16_t*>(dsm + kCFreq);
-  uint32_t* cum = reinterpret_cast<uint32_t*>(dsm + kCCum);
+  const unsigned long long* tab = reinterpret_cast<const unsigned long long*>(dsm + kCTab);
+  const uint16_t* freq = reinterpret_cast<const uint16_t*>(dsm + kCFreq);
   uint32_t* hist = reinterpret_cast<uint32_t*>(dsm + kCHist);
   uint32_t* rsize = reinterpret_cast<uint32_t*>(dsm + kCSize);
   uint32_t* rpre = reinterpret_cast<uint32_t*>(dsm + kCPre);
-  unsigned long long* red = reinterpret_cast<unsigned long long*>(dsm + kCRed);
-  uint8_t* ws = dsm + kRansMetaBytes;  // values [2 TE]
-  uint8_t* cs = ws + 2 * TE;           // cached exponents, then sign+mantissa bytes [TE]
-  uint8_t* scr = cs + TE;              // one record buffer per block [T * BB]
+  uint32_t* red = reinterpret_cast<uint32_t*>(dsm + kCRed);
+  uint32_t* fw = reinterpret_cast<uint32_t*>(dsm + kCFw);
+  uint8_t* ws = dsm + kRansEncMeta;  // values [2 TE]
+  uint8_t* cs = ws + 2 * TE;         // cached exponents, then sign+mantissa bytes [TE]
+  uint8_t* scr = cs + TE;            // one record buffer per block [T * BB]
   const int64_t LW = rans_lane_words(B);
   const int64_t BB = rans_block_bytes(B);
 
@@ -308,13 +342,13 @@ __global__ void __launch_bounds__(kThreads)
   if (tid == 0) {
     mbar_init(&bar, 1);
     fence_barrier_init();
-    mbar_arrive_expect_tx(&bar, 3u * te);
+    mbar_arrive_expect_tx(&bar, 3u * te + static_cast<uint32_t>(kRansEncTableBytes));
     bulk_g2s(ws, w, 2u * te, &bar);
     bulk_g2s(cs, c, te, &bar);
+    bulk_g2s(dsm + kCTab, enc_tables + kRansEncTableBytes * static_cast<int64_t>(x.rl),
+             static_cast<uint32_t>(kRansEncTableBytes), &bar);
   }
   __syncthreads();
-  // this shard's table, from its exponent histogram one iteration earlier
-  build_table(hist_prev + 256 * static_cast<int64_t>(x.rl), freq, cum, red);
 
   const int ngroups = static_cast<int>(te >> 4);
   if (warp == 0) {
@@ -340,7 +374,7 @@ __global__ void __launch_bounds__(kThreads)
     for (int g0 = ft - lane; g0 < ngroups; g0 += kThreads - 32) {
       const int gi = g0 + lane;
       const bool in = gi < ngroups;
-      uint32_t e[4] = {0x100u, 0x100u, 0x100u, 0x100u};
+      uint32_t e[4] = {0u, 0u, 0u, 0u};
       if (in) {
         const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
         const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
@@ -387,7 +421,7 @@ __global__ void __launch_bounds__(kThreads)
         if (i % (kThreads / 32 - 1) == warp - 1) {
           const int64_t L = (kb + 1) * B < x.te ? B : x.te - kb * B;
           const uint32_t units =
-              rans_encode_block(reinterpret_cast<const uint16_t*>(ws) + kb * B, L, freq, cum,
+              rans_encode_block(reinterpret_cast<const uint16_t*>(ws) + kb * B, L, tab,
                                 reinterpret_cast<uint16_t*>(scr + kb * BB), LW, lane);
           if (lane == 0) rsize[kb] = units;
         }
@@ -479,7 +513,10 @@ __global__ void __launch_bounds__(kThreads)
       if (!raw) payload[Ly.A + i] = static_cast<uint8_t>(byte);
     }
     if (to) record_status(p.ctl, kStatusTimeout);
-    const uint32_t n_changed = static_cast<uint32_t>(block_sum(nch, red));
+    const uint32_t tot = warp_sum(nch);
+    if (lane == 0) red[warp] = tot;
+    __syncthreads();
+    const uint32_t n_changed = red[0] + red[1] + red[2] + red[3];
     if (!raw) {
       for (int s = tid; s < 256; s += blockDim.x)
         reinterpret_cast<uint16_t*>(payload + Ly.C)[s] = freq[s];
@@ -512,7 +549,40 @@ __global__ void __launch_bounds__(kThreads) k_rans_raw_fixup(const CompressParam
   for (int64_t i = threadIdx.x; i < x.te / 8; i += blockDim.x) dst[i] = w[i];
 }
 
-__global__ void __launch_bounds__(kThreads) k_decompress_rans(const DecompressParams p) {
+// One CTA per rank (RANS ranks only, after the bitmap scan has validated the
+// frequencies): slot j -> symbol s with cum[s] <= j < cum[s+1], its
+// frequency and j - cum[s].
+__global__ void __launch_bounds__(kTableThreads)
+    k_rans_dec_tables(const DecompressParams p, uint32_t* __restrict__ tables) {
+  __shared__ unsigned long long red[kTableThreads / 32];
+  __shared__ uint32_t cum[257];
+  const int r = blockIdx.x;
+  if (p.rank_state[r] != kRankRans) return;
+  const int s = threadIdx.x;
+  const int64_t len = shard_len_of(p.geo, r);
+  const int64_t nb = (len + p.geo.B - 1) / p.geo.B;
+  const uint8_t* tab = p.payloads + static_cast<int64_t>(r) * p.stride + rans_layout(len, nb).C;
+  const uint32_t f = tab[2 * s] | (static_cast<uint32_t>(tab[2 * s + 1]) << 8);
+  const uint32_t c = table_exclusive_scan(f, red);
+  cum[s] = c;
+  if (s == kTableThreads - 1) cum[256] = c + f;
+  __syncthreads();
+  uint32_t* out = tables + 4096 * static_cast<int64_t>(r);
+  const uint32_t j0 = 16u * s;  // this thread's slots j0 .. j0+15
+  int lo = 0, hi = 255;         // largest symbol with cum <= j0
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cum[mid] <= j0) lo = mid; else hi = mid - 1;
+  }
+  uint32_t sym = static_cast<uint32_t>(lo);
+  for (uint32_t j = j0; j < j0 + 16; ++j) {
+    while (sym < 255 && cum[sym + 1] <= j) ++sym;
+    out[j] = sym | ((cum[sym + 1] - cum[sym]) << 8) | ((j - cum[sym]) << 20);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+    k_decompress_rans(const DecompressParams p, const uint32_t* __restrict__ dec_tables) {
   extern __shared__ __align__(128) uint8_t dsm[];
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t s_fw, s_bad;
@@ -528,15 +598,11 @@ __global__ void __launch_bounds__(kThreads) k_decompress_rans(const DecompressPa
     if (tid == 0) atomicOr(&p.ctl->status, kStatusInternal);
     return;
   }
-  uint16_t* freq = reinterpret_cast<uint16_t*>(dsm + kDFreq);
-  uint32_t* cum = reinterpret_cast<uint32_t*>(dsm + kDCum);
   uint32_t* offs = reinterpret_cast<uint32_t*>(dsm + kDOffs);
-  unsigned long long* red = reinterpret_cast<unsigned long long*>(dsm + kDRed);
-  uint8_t* slot_sym = dsm + kDSlot;
-  uint8_t* ss = dsm + kRansMetaBytes;  // sign+mantissa bytes [TE]
-  uint8_t* cs = ss + TE;               // exponents: cached, then decoded [TE]
-  uint8_t* ws = cs + TE;               // merged values [2 TE]
-  uint8_t* recs = ws + 2 * TE;         // records [T * BB]
+  uint32_t* tab = reinterpret_cast<uint32_t*>(dsm + kRansDecMeta);  // slot table
+  uint8_t* ss = dsm + kRansDecMeta + kRansDecTableBytes;  // sign+mantissa bytes [TE]
+  uint8_t* cs = ss + TE;              // exponents: cached, then decoded [TE]
+  uint8_t* recs = cs + TE;            // records [T * BB]
   const int64_t BB = rans_block_bytes(B);
   const ciera_desc d = p.descs[x.rl];
   const uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
@@ -570,7 +636,7 @@ __global__ void __launch_bounds__(kThreads) k_decompress_rans(const DecompressPa
       }
       bytes += b - a;
     }
-    if (fw) bytes += 512u;
+    if (fw) bytes += static_cast<uint32_t>(kRansDecTableBytes);
     s_fw = fw;
     s_bad = bad;
     mbar_init(&bar, 1);
@@ -579,7 +645,8 @@ __global__ void __launch_bounds__(kThreads) k_decompress_rans(const DecompressPa
     bulk_g2s(ss, payload + x.e0, te, &bar);
     bulk_g2s(cs, rc, te, &bar);
     if (fw) {
-      bulk_g2s(freq, payload + Ly.C, 512u, &bar);
+      bulk_g2s(tab, dec_tables + 4096 * static_cast<int64_t>(x.rl),
+               static_cast<uint32_t>(kRansDecTableBytes), &bar);
       for (int kb = 0; kb < x.nblk; ++kb)
         if ((fw >> kb) & 1u)
           bulk_g2s(recs + kb * BB, payload + Ly.D + offs[kb], offs[kb + 1] - offs[kb], &bar);
@@ -594,67 +661,31 @@ __global__ void __launch_bounds__(kThreads) k_decompress_rans(const DecompressPa
   }
   const uint32_t fw = s_fw;
   bool ok = true;
-  if (fw) {
-    // cumulative table (validated by the bitmap scan) and slot -> symbol
-    // map: thread t fills slots 32t .. 32t+31
-    const uint32_t f0 = freq[2 * tid], f1 = freq[2 * tid + 1];
-    const uint32_t c0 = block_exclusive_scan(f0 + f1, red);
-    cum[2 * tid] = c0;
-    cum[2 * tid + 1] = c0 + f0;
-    if (tid == kThreads - 1) cum[256] = c0 + f0 + f1;
-    __syncthreads();
-    const uint32_t j0 = 32u * tid;
-    int lo = 0, hi = 255;  // the symbol of slot j0: largest s with cum[s] <= j0
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (cum[mid] <= j0) lo = mid; else hi = mid - 1;
+  // decode: the i-th changed block goes to warp i % 4
+  int i = 0;
+  for (int kb = 0; kb < x.nblk; ++kb) {
+    if (!((fw >> kb) & 1u)) continue;
+    if (i % (kThreads / 32) == warp) {
+      const int64_t L = (kb + 1) * B < x.te ? B : x.te - kb * B;
+      ok = rans_decode_block(reinterpret_cast<const uint16_t*>(recs + kb * BB),
+                             (offs[kb + 1] - offs[kb]) / 2, L, tab, cs + kb * B, lane) && ok;
     }
-    uint32_t sym = static_cast<uint32_t>(lo);
-    for (int q = 0; q < 8; ++q) {
-      uint32_t word = 0;
-      for (int b = 0; b < 4; ++b) {
-        const uint32_t j = j0 + 4 * q + b;
-        while (sym < 255 && cum[sym + 1] <= j) ++sym;
-        word |= sym << (8 * b);
-      }
-      reinterpret_cast<uint32_t*>(slot_sym)[8 * tid + q] = word;
-    }
-    __syncthreads();
-    // decode: the i-th changed block goes to warp i % 4
-    int i = 0;
-    for (int kb = 0; kb < x.nblk; ++kb) {
-      if (!((fw >> kb) & 1u)) continue;
-      if (i % (kThreads / 32) == warp) {
-        const int64_t L = (kb + 1) * B < x.te ? B : x.te - kb * B;
-        ok = rans_decode_block(reinterpret_cast<const uint16_t*>(recs + kb * BB),
-                               (offs[kb + 1] - offs[kb]) / 2, L, freq, cum, slot_sym,
-                               cs + kb * B, lane) && ok;
-      }
-      ++i;
-    }
+    ++i;
   }
   const uint32_t any_bad = __syncthreads_or(!ok);
   if (tid == 0 && (any_bad || s_bad)) atomicOr(&p.ctl->status, kStatusCorrupt);
-  // merge; ExpCache refresh of the changed blocks
+  // merge straight to the output; ExpCache refresh of the changed blocks
+  uint4* out = reinterpret_cast<uint4*>(p.out + x.shard_off + x.e0);
   const int ngroups = static_cast<int>(te >> 4);
   for (int gi = tid; gi < ngroups; gi += blockDim.x) {
     const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
     const uint4 s = reinterpret_cast<const uint4*>(ss)[gi];
     const uint4 e = reinterpret_cast<const uint4*>(cs)[gi];
-    reinterpret_cast<uint4*>(ws)[2 * gi] =
-        make_uint4(join2(s.x, e.x), join2(s.x >> 16, e.x >> 16), join2(s.y, e.y),
-                   join2(s.y >> 16, e.y >> 16));
-    reinterpret_cast<uint4*>(ws)[2 * gi + 1] =
-        make_uint4(join2(s.z, e.z), join2(s.z >> 16, e.z >> 16), join2(s.w, e.w),
-                   join2(s.w >> 16, e.w >> 16));
+    out[2 * gi] = make_uint4(join2(s.x, e.x), join2(s.x >> 16, e.x >> 16), join2(s.y, e.y),
+                             join2(s.y >> 16, e.y >> 16));
+    out[2 * gi + 1] = make_uint4(join2(s.z, e.z), join2(s.z >> 16, e.z >> 16), join2(s.w, e.w),
+                                 join2(s.w >> 16, e.w >> 16));
     if ((fw >> kb) & 1u) reinterpret_cast<uint4*>(rc)[gi] = e;
-  }
-  fence_proxy_async_smem();
-  __syncthreads();
-  if (tid == 0) {
-    bulk_s2g(p.out + x.shard_off + x.e0, ws, 2u * te);
-    bulk_commit();
-    bulk_wait_read_all();
   }
 }
 
@@ -680,14 +711,18 @@ cudaError_t allow_smem(const void* fn, int64_t bytes, std::atomic<int64_t>* done
 }  // namespace
 
 int launch_compress_rans(const CompressParams& p, const uint32_t* hist_prev, uint32_t* hist_out,
-                         void* stream) {
+                         uint8_t* enc_tables, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t smem = rans_compress_smem(p.geo.T, p.geo.B);
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(k_compress_rans), smem, g_smem_c);
   if (e != cudaSuccess) return e;
+  k_rans_enc_tables<<<static_cast<unsigned>(p.geo.rank_count), kTableThreads, 0, s>>>(
+      hist_prev, enc_tables);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   const int64_t grid = p.geo.total_tiles + 1;
   k_compress_rans<<<static_cast<unsigned>(grid), kThreads, static_cast<size_t>(smem), s>>>(
-      p, hist_prev, hist_out);
+      p, enc_tables, hist_out);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (!(p.flags & CIERA_COLD) && p.geo.total_tiles > 0) {
@@ -697,14 +732,18 @@ int launch_compress_rans(const CompressParams& p, const uint32_t* hist_prev, uin
   return e;
 }
 
-int launch_decompress_rans(const DecompressParams& p, void* stream) {
+int launch_decompress_rans(const DecompressParams& p, uint32_t* dec_tables, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p.geo.total_tiles <= 0) return cudaSuccess;
   const int64_t smem = rans_decompress_smem(p.geo.T, p.geo.B);
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(k_decompress_rans), smem, g_smem_d);
   if (e != cudaSuccess) return e;
+  k_rans_dec_tables<<<static_cast<unsigned>(p.geo.rank_count), kTableThreads, 0, s>>>(
+      p, dec_tables);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   k_decompress_rans<<<static_cast<unsigned>(p.geo.total_tiles), kThreads,
-                      static_cast<size_t>(smem), s>>>(p);
+                      static_cast<size_t>(smem), s>>>(p, dec_tables);
   return cudaGetLastError();
 }
 

@@ -19,20 +19,31 @@ __host__ __device__ inline int64_t rans_block_bytes(int64_t B) {
   return 2 * (kRansLanes + kRansLanes * rans_lane_words(B));
 }
 
-// Dynamic shared memory of the RANS kernels for tiles of T blocks of B.
-constexpr int64_t kRansMetaBytes = 8192;  // tables, counters (see ciera_rans.cu)
+// Per-rank coder tables in the workspace.
+//   encoder: 256 packed uint64 entries (division constants, cumulative
+//            frequency, complement), then the 256 uint16 frequencies
+//   decoder: 4096 uint32 slot entries (symbol, frequency, slot bias)
+constexpr int64_t kRansEncTableBytes = 256 * 8 + 256 * 2;
+constexpr int64_t kRansDecTableBytes = 4096 * 4;
+
+// Dynamic shared memory of the RANS tile kernels for tiles of T blocks of B.
+constexpr int64_t kRansEncMeta = 4096;  // coder table, histogram, sizes (ciera_rans.cu)
+constexpr int64_t kRansDecMeta = 1024;  // offsets, reductions
 __host__ __device__ inline int64_t rans_compress_smem(int64_t T, int64_t B) {
-  return kRansMetaBytes + 3 * T * B + T * rans_block_bytes(B);
+  return kRansEncMeta + 3 * T * B + T * rans_block_bytes(B);
 }
 __host__ __device__ inline int64_t rans_decompress_smem(int64_t T, int64_t B) {
-  return kRansMetaBytes + 4 * T * B + T * rans_block_bytes(B);
+  return kRansDecMeta + kRansDecTableBytes + 2 * T * B + T * rans_block_bytes(B);
 }
 
-// Launchers (ciera_rans.cu), returning a cudaError_t value: the RANS sender
-// (hist_prev/hist_out: 256 uint32 per rank of the range) and the RANS part
-// of the receiver.
+// Launchers (ciera_rans.cu), returning a cudaError_t value.
+//   launch_compress_rans: the RANS sender; hist_prev/hist_out hold 256
+//     uint32 per rank of the range (hist_out zeroed by the caller),
+//     enc_tables kRansEncTableBytes per rank of the range.
+//   launch_decompress_rans: the RANS part of the receiver, after the bitmap
+//     scan; dec_tables kRansDecTableBytes per rank.
 int launch_compress_rans(const CompressParams& p, const uint32_t* hist_prev, uint32_t* hist_out,
-                         void* stream);
-int launch_decompress_rans(const DecompressParams& p, void* stream);
+                         uint8_t* enc_tables, void* stream);
+int launch_decompress_rans(const DecompressParams& p, uint32_t* dec_tables, void* stream);
 
 }  // namespace ciera
