@@ -198,10 +198,12 @@ int ciera_compress_hashed(ciera_plan_t plan, int rank_begin, int rank_count,
  * ciera_compress when cold, or when the RANS payload would not be smaller
  * than 2*len.
  *   hist_prev_dev  rank_count rows of 256 uint32: the histogram of each
- *                  shard's exponents one call earlier (zeros at first)
+ *                  shard's sampled exponents one call earlier (zeros at
+ *                  first); the sample is every 16th value of the shard
+ *                  (positions 0, 16, 32, ...)
  *   hist_out_dev   rank_count rows of 256 uint32, overwritten with the
- *                  histogram of this call's exponents (the next call's
- *                  hist_prev); must not overlap hist_prev_dev
+ *                  histogram of this call's sampled exponents (the next
+ *                  call's hist_prev); must not overlap hist_prev_dev
  * Other arguments as ciera_compress.  Errors: as ciera_compress, and
  * CIERA_E_INVAL unless the plan takes the fast path, N is a multiple of 16,
  * S <= 2^30, and w_dev, sender_cache_dev, payloads_dev (and the stride) are

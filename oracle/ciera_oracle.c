@@ -717,8 +717,11 @@ int oracle_rans_decode_block(const uint8_t *rec, int64_t rec_bytes, int64_t L,
  *   D = align16(O + 4 (n_b + 1))  the records of the changed blocks, in order
  * Descriptor: mode 2, body_bytes = D, payload_bytes = D + records.  RAW as
  * before when cold, empty, or when the payload would not be smaller than
- * 2*len.  hist_prev: histogram of the shard's exponents one iteration
- * earlier (the table's source); hist_cur: output, this iteration's. */
+ * 2*len.  hist_prev: histogram of the shard's sampled exponents one
+ * iteration earlier (the table's source); hist_cur: output, this
+ * iteration's.  The sample is every 16th value of the shard (positions 0,
+ * 16, 32, ...): the table needs the exponents' distribution, not every
+ * count, and a sixteenth of a shard still holds thousands of values. */
 int oracle_compress_shard_rans(const uint16_t *shard, int64_t len, int64_t block,
                                uint8_t *sender_cache, int cold, const uint32_t *hist_prev,
                                uint32_t *hist_cur, uint8_t *payload, uint8_t *flags_out,
@@ -740,7 +743,7 @@ int oracle_compress_shard_rans(const uint16_t *shard, int64_t len, int64_t block
     for (j = 0; j < 256; ++j) {
         hist_cur[j] = 0;
     }
-    for (j = 0; j < len; ++j) {
+    for (j = 0; j < len; j += 16) {
         hist_cur[oracle_exp(shard[j])] += 1;
     }
     /* flags: the exact change test */

@@ -100,7 +100,8 @@ def test_rans_shard_round_trip(block, p_block):
         payload, flags, d, hist_next = oracle.compress_shard_rans(w, block, sc, t == 0, hist)
         _, flags_exact, d_exact = oracle.compress_shard(w, block, sc_exact, t == 0)
         np.testing.assert_array_equal(flags, flags_exact)
-        np.testing.assert_array_equal(hist_next, np.bincount(_exps(w), minlength=256))
+        # the table's source: every 16th exponent of the shard
+        np.testing.assert_array_equal(hist_next, np.bincount(_exps(w)[::16], minlength=256))
         np.testing.assert_array_equal(sc, _exps(w))
         st, out = oracle.decompress_shard_any(payload, d, n, block, rc)
         assert st == 0
