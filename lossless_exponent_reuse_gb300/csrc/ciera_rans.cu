@@ -18,7 +18,8 @@
 //   D          records of the changed blocks: 32 uint16 lane word counts,
 //              then the lanes' words in decoding order, padded to 16 bytes
 // The table is normalised from the histogram of the shard's exponents one
-// iteration earlier, which the previous call accumulated as a by-product.
+// iteration earlier (every 16th value), which the previous call accumulated
+// as a by-product.
 //
 // Kernels:
 //   k_rans_enc_tables  one CTA per rank: frequencies from the histogram, and
@@ -26,10 +27,11 @@
 //                      frequency (Granlund and Montgomery, "Division by
 //                      invariant integers using multiplication", 1994), so
 //                      that a coding step multiplies instead of dividing.
-//   k_compress_rans    one CTA per tile, ticket order: flags (exact test)
-//                      and the exponent histogram, cache refresh, sign+
-//                      mantissa bytes to their fixed positions, one warp
-//                      per changed block codes it, decoupled look-back over
+//   k_compress_rans    one CTA per tile, ticket order: one streaming pass
+//                      (flags by the exact test, cache refresh, sign+mantissa
+//                      bytes to their fixed positions, the tile's exponents
+//                      into shared memory, the sampled histogram); one warp
+//                      per changed block codes it; decoupled look-back over
 //                      the record sizes places the records.
 //   k_rans_raw_fixup   rewrites a shard raw when its RANS payload would not
 //                      have been smaller than the raw bytes.
@@ -37,9 +39,10 @@
 //                      bias) table of 4096 entries from the received
 //                      frequencies, so that a decoding step is one lookup.
 //   k_decompress_rans  one CTA per tile of a RANS rank: bulk copies of the
-//                      sign+mantissa bytes, cached exponents, slot table and
-//                      records; one warp per changed block decodes it; merge
-//                      straight to the output; ExpCache refresh.
+//                      sign+mantissa bytes and the records; the kept blocks
+//                      merge with their cached exponents; one warp per
+//                      changed block decodes it (slot table read through
+//                      L1) straight into the output and the ExpCache.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -161,19 +164,19 @@ __global__ void __launch_bounds__(kTableThreads)
 // counts at rec[0..31], lane regions of LW words from rec[32]; then the
 // streams are compacted in place behind the counts and padded to 16 bytes.
 // Returns the record size in 16-byte units.
-__device__ uint32_t rans_encode_block(const uint16_t* vals, int64_t L,
-                                      const unsigned long long* tab, uint16_t* rec, int64_t LW,
+__device__ uint32_t rans_encode_block(const uint8_t* exps, int L,
+                                      const unsigned long long* tab, uint16_t* rec, int LW,
                                       int lane) {
   uint16_t* region = rec + kRansLanes + lane * LW;
-  int64_t top = LW;
+  int top = LW;
   uint32_t x = kRansLow;
   if (lane < L) {
-    int64_t j = lane + ((L - 1 - lane) / kRansLanes) * kRansLanes;
-    unsigned long long E = tab[exp1(vals[j])];
+    int j = lane + ((L - 1 - lane) / kRansLanes) * kRansLanes;
+    unsigned long long E = tab[exps[j]];
     for (;;) {
       // the next symbol's entry is loaded while this one is coded
-      const int64_t jn = j - kRansLanes;
-      const unsigned long long En = jn >= 0 ? tab[exp1(vals[jn])] : 0ull;
+      const int jn = j - kRansLanes;
+      const unsigned long long En = jn >= 0 ? tab[exps[jn]] : 0ull;
       const uint32_t m = static_cast<uint32_t>(E);
       const uint32_t hi = static_cast<uint32_t>(E >> 32);
       const uint32_t c = hi & 0xFFFu;
@@ -210,8 +213,8 @@ __device__ uint32_t rans_encode_block(const uint16_t* vals, int64_t L,
   for (int l = 0; l < kRansLanes; ++l) {
     const uint32_t n = __shfl_sync(0xffffffffu, nw, l);
     const uint32_t p0 = __shfl_sync(0xffffffffu, pre, l);
-    const int64_t src = kRansLanes + l * LW + (LW - n);
-    const int64_t dst = kRansLanes + p0;
+    const int src = kRansLanes + l * LW + (LW - static_cast<int>(n));
+    const int dst = kRansLanes + static_cast<int>(p0);
     for (uint32_t c = 0; c < n; c += 32) {
       const bool ok = c + lane < n;
       uint16_t v = 0;
@@ -228,11 +231,14 @@ __device__ uint32_t rans_encode_block(const uint16_t* vals, int64_t L,
   return padded / 8u;
 }
 
-// One warp decodes one record of `rec_words` words into L exponents with the
-// slot table `tab` (entry: symbol | f << 8 | (slot - cum) << 20).  False
-// (for the whole warp) if the record does not decode cleanly.
-__device__ bool rans_decode_block(const uint16_t* rec, uint32_t rec_words, int64_t L,
-                                  const uint32_t* tab, uint8_t* exps, int lane) {
+// One warp decodes one record of `rec_words` words into the block's L
+// exponents with the slot table `tab` (entry: symbol | f << 8 | (slot - cum)
+// << 20, read through L1), and writes each value (joined with its
+// sign+mantissa byte from `ss`) to `out` and its exponent to the ExpCache
+// `rc`.  False (for the whole warp) if the record does not decode cleanly.
+__device__ bool rans_decode_block(const uint16_t* rec, uint32_t rec_words, int L,
+                                  const uint32_t* __restrict__ tab, const uint8_t* ss,
+                                  uint16_t* out, uint8_t* rc, int lane) {
   const uint32_t nw = rec_words >= kRansLanes ? rec[lane] : 0u;
   uint32_t incl = nw;
 #pragma unroll
@@ -248,9 +254,11 @@ __device__ bool rans_decode_block(const uint16_t* rec, uint32_t rec_words, int64
   uint32_t x = (static_cast<uint32_t>(s[0]) << 16) | s[1];
   uint32_t idx = 2;
   uint32_t nxt = idx < nw ? s[idx] : 0u;  // the next renormalisation word, loaded ahead
-  for (int64_t j = lane; j < L; j += kRansLanes) {
-    const uint32_t e = tab[x & (kRansTotal - 1)];
-    exps[j] = static_cast<uint8_t>(e);
+  for (int j = lane; j < L; j += kRansLanes) {
+    const uint32_t e = __ldg(tab + (x & (kRansTotal - 1)));
+    const uint32_t sym = e & 0xFFu;
+    out[j] = static_cast<uint16_t>(join1(ss[j], sym));
+    rc[j] = static_cast<uint8_t>(sym);
     x = ((e >> 8) & 0xFFFu) * (x >> kRansBits) + (e >> 20);
     if (x < kRansLow) {
       if (idx >= nw) {
@@ -271,7 +279,6 @@ struct RansShared {
   uint32_t epoch;  // this launch's tag of look-back and flag words
   uint32_t X;      // record units (16 bytes) before the tile in its shard
   uint32_t agg;    // record units of the tile
-  uint32_t bad;    // a bounded wait ran out on this tile
 };
 
 __global__ void __launch_bounds__(kThreads)
@@ -292,9 +299,8 @@ __global__ void __launch_bounds__(kThreads)
   uint32_t* rpre = reinterpret_cast<uint32_t*>(dsm + kCPre);
   uint32_t* red = reinterpret_cast<uint32_t*>(dsm + kCRed);
   uint32_t* fw = reinterpret_cast<uint32_t*>(dsm + kCFw);
-  uint8_t* ws = dsm + kRansEncMeta;  // values [2 TE]
-  uint8_t* cs = ws + 2 * TE;         // cached exponents, then sign+mantissa bytes [TE]
-  uint8_t* scr = cs + TE;            // one record buffer per block [T * BB]
+  uint8_t* es = dsm + kRansEncMeta;  // the tile's exponents [TE]
+  uint8_t* scr = es + TE;            // one coding buffer per block [T * BB]
   const int64_t LW = rans_lane_words(B);
   const int64_t BB = rans_block_bytes(B);
 
@@ -306,7 +312,6 @@ __global__ void __launch_bounds__(kThreads)
       atomicExch(&p.ctl->ticket, static_cast<unsigned long long>(launch + 1u) << 32);
     sh.ticket = t;
     sh.epoch = launch % 0xffffffffu + 1u;
-    sh.bad = 0;
     fw[0] = 0;
   }
   if (dynamic_smem_size() < static_cast<uint32_t>(rans_compress_smem(T, B)) || T > 32 ||
@@ -336,21 +341,23 @@ __global__ void __launch_bounds__(kThreads)
   // a shard whose sections alone are not smaller than its raw bytes, or a
   // cold one, goes out raw whatever its records would be
   const bool direct_raw = cold || Ly.D >= 2 * x.len;
-  const uint16_t* w = p.w + x.shard_off + x.e0;
-  uint8_t* c = p.scache + x.shard_off + x.e0;
+  const uint4* w4 = reinterpret_cast<const uint4*>(p.w + x.shard_off + x.e0);
+  uint4* c4 = reinterpret_cast<uint4*>(p.scache + x.shard_off + x.e0);
+  uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
   const uint32_t te = static_cast<uint32_t>(x.te);
   if (tid == 0) {
+    // this shard's coder table (written by k_rans_enc_tables)
     mbar_init(&bar, 1);
     fence_barrier_init();
-    mbar_arrive_expect_tx(&bar, 3u * te + static_cast<uint32_t>(kRansEncTableBytes));
-    bulk_g2s(ws, w, 2u * te, &bar);
-    bulk_g2s(cs, c, te, &bar);
+    mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(kRansEncTableBytes));
     bulk_g2s(dsm + kCTab, enc_tables + kRansEncTableBytes * static_cast<int64_t>(x.rl),
              static_cast<uint32_t>(kRansEncTableBytes), &bar);
   }
   __syncthreads();
 
   const int ngroups = static_cast<int>(te >> 4);
+  // block of group gi: gi / (B/16), as mulhi(gi, ceil(2^32 / (B/16))), exact for gi < 2^16
+  const uint32_t mG = static_cast<uint32_t>(((1ull << 32) + B / 16 - 1) / (B / 16));
   if (warp == 0) {
     bool to = false;
     const uint32_t X =
@@ -361,68 +368,59 @@ __global__ void __launch_bounds__(kThreads)
     }
   } else {
     const int ft = tid - 32;
-    if (!mbar_wait_bounded(&bar, 0, p.timeout_ns)) {
-      record_status(p.ctl, kStatusTimeout);
-      sh.bad = 1;
-      mbar_wait_bounded(&bar, 0, p.timeout_ns);
-    }
-    flaggers_sync();
-    const bool all = cold || sh.bad;
-    // flags (exact test) and the tile's exponent histogram; the loop runs
-    // whole warps so that equal exponents can be merged across lanes
+    // One streaming pass over the tile, 16 values per thread and step:
+    // flags (exact test), sender-cache refresh of the groups that differ,
+    // the payload's bytes (sign+mantissa, or raw values), the exponents for
+    // the coder, and the sampled histogram (the first value of each group).
+    // The loop runs whole warps so that equal samples merge across lanes.
     uint32_t mine = 0;
     for (int g0 = ft - lane; g0 < ngroups; g0 += kThreads - 32) {
       const int gi = g0 + lane;
       const bool in = gi < ngroups;
-      uint32_t e[4] = {0u, 0u, 0u, 0u};
+      uint32_t sample = 0x100u + lane;
       if (in) {
-        const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
-        const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
-        const uint4 cc = reinterpret_cast<const uint4*>(cs)[gi];
-        e[0] = exp4(w0.x, w0.y);
-        e[1] = exp4(w0.z, w0.w);
-        e[2] = exp4(w1.x, w1.y);
-        e[3] = exp4(w1.z, w1.w);
-        const uint32_t d = (e[0] ^ cc.x) | (e[1] ^ cc.y) | (e[2] ^ cc.z) | (e[3] ^ cc.w);
-        if (d || all) mine |= 1u << static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
+        const uint4 w0 = __ldg(w4 + 2 * gi);
+        const uint4 w1 = __ldg(w4 + 2 * gi + 1);
+        const uint4 cc = c4[gi];
+        const uint4 e = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w), exp4(w1.x, w1.y),
+                                   exp4(w1.z, w1.w));
+        const uint32_t d = (e.x ^ cc.x) | (e.y ^ cc.y) | (e.z ^ cc.z) | (e.w ^ cc.w);
+        if (d || cold) {
+          mine |= 1u << __umulhi(static_cast<uint32_t>(gi), mG);
+          c4[gi] = e;
+        }
+        reinterpret_cast<uint4*>(es)[gi] = e;
+        if (direct_raw) {
+          uint4* dst = reinterpret_cast<uint4*>(payload + 2 * x.e0) + 2 * gi;
+          dst[0] = w0;
+          dst[1] = w1;
+        } else {
+          reinterpret_cast<uint4*>(payload + x.e0)[gi] =
+              make_uint4(sm4(w0.x, w0.y), sm4(w0.z, w0.w), sm4(w1.x, w1.y), sm4(w1.z, w1.w));
+        }
+        sample = e.x & 0xFFu;
       }
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const uint32_t v = in ? (e[q >> 2] >> (8 * (q & 3))) & 0xFFu : 0x100u + lane;
-        const uint32_t same = __match_any_sync(0xffffffffu, v);
-        if (in && lane == __ffs(same) - 1) atomicAdd(&hist[v], static_cast<uint32_t>(__popc(same)));
-      }
+      const uint32_t same = __match_any_sync(0xffffffffu, sample);
+      if (in && lane == __ffs(same) - 1) atomicAdd(&hist[sample], static_cast<uint32_t>(__popc(same)));
     }
     mine = __reduce_or_sync(0xffffffffu, mine);
     if (lane == 0 && mine) atomicOr(&fw[0], mine);
+    if (!mbar_wait_bounded(&bar, 0, p.timeout_ns)) {
+      record_status(p.ctl, kStatusTimeout);
+      mbar_wait_bounded(&bar, 0, p.timeout_ns);
+    }
     flaggers_sync();
     const uint32_t f = fw[0];
-    // sender cache of changed blocks; every value's sign+mantissa byte into cs
-    for (int gi = ft; gi < ngroups; gi += kThreads - 32) {
-      const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
-      const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
-      const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
-      if ((f >> kb) & 1u) {
-        const uint4 e = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w), exp4(w1.x, w1.y),
-                                   exp4(w1.z, w1.w));
-        const uint4 cc = reinterpret_cast<const uint4*>(cs)[gi];
-        if (all || ((e.x ^ cc.x) | (e.y ^ cc.y) | (e.z ^ cc.z) | (e.w ^ cc.w)))
-          reinterpret_cast<uint4*>(c)[gi] = e;
-      }
-      if (!direct_raw)
-        reinterpret_cast<uint4*>(cs)[gi] =
-            make_uint4(sm4(w0.x, w0.y), sm4(w0.z, w0.w), sm4(w1.x, w1.y), sm4(w1.z, w1.w));
-    }
     // code the changed blocks: the i-th changed block goes to warp 1 + i % 3
     if (!direct_raw) {
       int i = 0;
       for (int kb = 0; kb < x.nblk; ++kb) {
         if (!((f >> kb) & 1u)) continue;
         if (i % (kThreads / 32 - 1) == warp - 1) {
-          const int64_t L = (kb + 1) * B < x.te ? B : x.te - kb * B;
+          const int L = static_cast<int>((kb + 1) * B < x.te ? B : x.te - kb * B);
           const uint32_t units =
-              rans_encode_block(reinterpret_cast<const uint16_t*>(ws) + kb * B, L, tab,
-                                reinterpret_cast<uint16_t*>(scr + kb * BB), LW, lane);
+              rans_encode_block(es + kb * B, L, tab, reinterpret_cast<uint16_t*>(scr + kb * BB),
+                                static_cast<int>(LW), lane);
           if (lane == 0) rsize[kb] = units;
         }
         ++i;
@@ -450,18 +448,12 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   if (tid == 0 && x.t > 0 && !direct_raw) publish(p, x, sh.epoch, kStateInclusive, sh.X + sh.agg);
 
-  uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
   const int64_t limit = 2 * x.len;  // a payload this large goes out raw instead
-  if (tid == 0) {
-    if (direct_raw) {
-      bulk_s2g(payload + 2 * x.e0, ws, 2u * te);
-    } else {
-      bulk_s2g(payload + x.e0, cs, te);
-      for (int kb = 0; kb < x.nblk; ++kb) {
-        const int64_t at = Ly.D + 16 * static_cast<int64_t>(sh.X + rpre[kb]);
-        if (rsize[kb] && at + 16 * static_cast<int64_t>(rsize[kb]) <= limit)
-          bulk_s2g(payload + at, scr + kb * BB, 16u * rsize[kb]);
-      }
+  if (tid == 0 && !direct_raw) {
+    for (int kb = 0; kb < x.nblk; ++kb) {
+      const int64_t at = Ly.D + 16 * static_cast<int64_t>(sh.X + rpre[kb]);
+      if (rsize[kb] && at + 16 * static_cast<int64_t>(rsize[kb]) <= limit)
+        bulk_s2g(payload + at, scr + kb * BB, 16u * rsize[kb]);
     }
     bulk_commit();
   }
@@ -533,7 +525,7 @@ __global__ void __launch_bounds__(kThreads)
       p.descs[x.rl] = d;
     }
   }
-  if (tid == 0) bulk_wait_read_all();
+  if (tid == 0 && !direct_raw) bulk_wait_read_all();
 }
 
 // A shard that went raw only at the end (its RANS payload would not have
@@ -585,7 +577,7 @@ __global__ void __launch_bounds__(kThreads)
     k_decompress_rans(const DecompressParams p, const uint32_t* __restrict__ dec_tables) {
   extern __shared__ __align__(128) uint8_t dsm[];
   __shared__ __align__(8) uint64_t bar;
-  __shared__ uint32_t s_fw, s_bad;
+  __shared__ uint32_t s_fw, s_bad, s_staged;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const Tile x = decode_tile(p.geo, blockIdx.x);
@@ -599,15 +591,13 @@ __global__ void __launch_bounds__(kThreads)
     return;
   }
   uint32_t* offs = reinterpret_cast<uint32_t*>(dsm + kDOffs);
-  uint32_t* tab = reinterpret_cast<uint32_t*>(dsm + kRansDecMeta);  // slot table
-  uint8_t* ss = dsm + kRansDecMeta + kRansDecTableBytes;  // sign+mantissa bytes [TE]
-  uint8_t* cs = ss + TE;              // exponents: cached, then decoded [TE]
-  uint8_t* recs = cs + TE;            // records [T * BB]
-  const int64_t BB = rans_block_bytes(B);
+  uint8_t* ss = dsm + kRansDecMeta;   // sign+mantissa bytes [TE]
+  uint8_t* recs = ss + TE;            // the tile's records, when they fit [TE]
   const ciera_desc d = p.descs[x.rl];
   const uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
   const RansLayout Ly = rans_layout(x.len, x.nb);
   uint8_t* rc = p.rcache + x.shard_off + x.e0;
+  uint16_t* out = p.out + x.shard_off + x.e0;
   const uint32_t te = static_cast<uint32_t>(x.te);
   if (tid <= x.nblk) offs[tid] = reinterpret_cast<const uint32_t*>(payload + Ly.O)[x.k0 + tid];
   __syncthreads();
@@ -622,71 +612,93 @@ __global__ void __launch_bounds__(kThreads)
     uint32_t fw = static_cast<uint32_t>(two >> sh0) &
                   (x.nblk >= 32 ? 0xffffffffu : ((1u << x.nblk) - 1u));
     uint32_t bad = 0;
-    uint32_t bytes = 2u * te;
+    uint64_t rec_bytes = 0;
     for (int kb = 0; kb < x.nblk; ++kb) {
       if (!((fw >> kb) & 1u)) continue;
       const uint32_t a = offs[kb], b = offs[kb + 1];
-      // a record must be nonempty, lie inside the payload and, for the bulk
-      // copy, start and end on 16 bytes and fit its buffer
-      if (b <= a || (a & 15u) || (b & 15u) || b - a > BB ||
+      // a record must be nonempty, lie inside the payload and start and end
+      // on 16 bytes (the bulk copy's alignment)
+      if (b <= a || (a & 15u) || (b & 15u) ||
           static_cast<uint64_t>(Ly.D) + b > d.payload_bytes) {
         bad = 1;
         fw &= ~(1u << kb);
         continue;
       }
-      bytes += b - a;
+      rec_bytes += b - a;
     }
-    if (fw) bytes += static_cast<uint32_t>(kRansDecTableBytes);
+    // stage the records when they fit; else decode them from global memory
+    const bool staged = rec_bytes <= static_cast<uint64_t>(TE);
     s_fw = fw;
     s_bad = bad;
+    s_staged = staged;
     mbar_init(&bar, 1);
     fence_barrier_init();
-    mbar_arrive_expect_tx(&bar, bytes);
+    mbar_arrive_expect_tx(&bar, te + (staged ? static_cast<uint32_t>(rec_bytes) : 0u));
     bulk_g2s(ss, payload + x.e0, te, &bar);
-    bulk_g2s(cs, rc, te, &bar);
-    if (fw) {
-      bulk_g2s(tab, dec_tables + 4096 * static_cast<int64_t>(x.rl),
-               static_cast<uint32_t>(kRansDecTableBytes), &bar);
+    if (staged) {
+      uint32_t at = 0;
       for (int kb = 0; kb < x.nblk; ++kb)
-        if ((fw >> kb) & 1u)
-          bulk_g2s(recs + kb * BB, payload + Ly.D + offs[kb], offs[kb + 1] - offs[kb], &bar);
+        if ((fw >> kb) & 1u) {
+          bulk_g2s(recs + at, payload + Ly.D + offs[kb], offs[kb + 1] - offs[kb], &bar);
+          at += offs[kb + 1] - offs[kb];
+        }
     }
   }
   __syncthreads();
+  const uint32_t fw = s_fw;
+  // the kept blocks' cached exponents, read while the bulk copies land
+  const uint32_t mG = static_cast<uint32_t>(((1ull << 32) + B / 16 - 1) / (B / 16));
+  const int ngroups = static_cast<int>(te >> 4);
+  constexpr int kPer = 4;  // groups per thread held in registers before the merge
+  uint4 kept[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int gi = tid + q * kThreads;
+    if (gi < ngroups && !((fw >> __umulhi(static_cast<uint32_t>(gi), mG)) & 1u))
+      kept[q] = reinterpret_cast<const uint4*>(rc)[gi];
+  }
   if (__syncthreads_or(!mbar_wait_bounded(&bar, 0, p.timeout_ns))) {
     if (tid == 0) atomicOr(&p.ctl->status, kStatusTimeout);
     mbar_wait_bounded(&bar, 0, p.timeout_ns);
     __syncthreads();
     return;
   }
-  const uint32_t fw = s_fw;
+  // merge of the kept blocks: sign+mantissa bytes with cached exponents
+  for (int gi0 = 0; gi0 < ngroups; gi0 += kPer * kThreads) {
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int gi = gi0 + tid + q * kThreads;
+      if (gi >= ngroups || ((fw >> __umulhi(static_cast<uint32_t>(gi), mG)) & 1u)) continue;
+      const uint4 e = gi0 == 0 ? kept[q] : reinterpret_cast<const uint4*>(rc)[gi];
+      const uint4 s = reinterpret_cast<const uint4*>(ss)[gi];
+      uint4* o = reinterpret_cast<uint4*>(out) + 2 * gi;
+      o[0] = make_uint4(join2(s.x, e.x), join2(s.x >> 16, e.x >> 16), join2(s.y, e.y),
+                        join2(s.y >> 16, e.y >> 16));
+      o[1] = make_uint4(join2(s.z, e.z), join2(s.z >> 16, e.z >> 16), join2(s.w, e.w),
+                        join2(s.w >> 16, e.w >> 16));
+    }
+  }
+  // decode the changed blocks straight into the output and the ExpCache:
+  // the i-th changed block goes to warp i % 4
+  const bool staged = s_staged;
+  const uint32_t* tab = dec_tables + 4096 * static_cast<int64_t>(x.rl);
   bool ok = true;
-  // decode: the i-th changed block goes to warp i % 4
   int i = 0;
+  uint32_t at = 0;
   for (int kb = 0; kb < x.nblk; ++kb) {
     if (!((fw >> kb) & 1u)) continue;
+    const uint32_t nbytes = offs[kb + 1] - offs[kb];
     if (i % (kThreads / 32) == warp) {
-      const int64_t L = (kb + 1) * B < x.te ? B : x.te - kb * B;
-      ok = rans_decode_block(reinterpret_cast<const uint16_t*>(recs + kb * BB),
-                             (offs[kb + 1] - offs[kb]) / 2, L, tab, cs + kb * B, lane) && ok;
+      const int L = static_cast<int>((kb + 1) * B < x.te ? B : x.te - kb * B);
+      const uint8_t* rec = staged ? recs + at : payload + Ly.D + offs[kb];
+      ok = rans_decode_block(reinterpret_cast<const uint16_t*>(rec), nbytes / 2, L, tab,
+                             ss + kb * B, out + kb * B, rc + kb * B, lane) && ok;
     }
+    at += nbytes;
     ++i;
   }
   const uint32_t any_bad = __syncthreads_or(!ok);
   if (tid == 0 && (any_bad || s_bad)) atomicOr(&p.ctl->status, kStatusCorrupt);
-  // merge straight to the output; ExpCache refresh of the changed blocks
-  uint4* out = reinterpret_cast<uint4*>(p.out + x.shard_off + x.e0);
-  const int ngroups = static_cast<int>(te >> 4);
-  for (int gi = tid; gi < ngroups; gi += blockDim.x) {
-    const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
-    const uint4 s = reinterpret_cast<const uint4*>(ss)[gi];
-    const uint4 e = reinterpret_cast<const uint4*>(cs)[gi];
-    out[2 * gi] = make_uint4(join2(s.x, e.x), join2(s.x >> 16, e.x >> 16), join2(s.y, e.y),
-                             join2(s.y >> 16, e.y >> 16));
-    out[2 * gi + 1] = make_uint4(join2(s.z, e.z), join2(s.z >> 16, e.z >> 16), join2(s.w, e.w),
-                                 join2(s.w >> 16, e.w >> 16));
-    if ((fw >> kb) & 1u) reinterpret_cast<uint4*>(rc)[gi] = e;
-  }
 }
 
 constexpr int kMaxDevices = 64;

@@ -9,9 +9,11 @@
 namespace ciera {
 
 // uint16 words per lane region of a block's coding scratch: the final state
-// and at most one renormalisation word per symbol, rounded to 16 bytes.
+// and at most one renormalisation word per symbol, rounded up to 2 mod 4 so
+// that the lanes' regions start in 32 different shared-memory banks.
 __host__ __device__ inline int64_t rans_lane_words(int64_t B) {
-  return (2 + (B + kRansLanes - 1) / kRansLanes + 7) & ~int64_t(7);
+  const int64_t need = 2 + (B + kRansLanes - 1) / kRansLanes;
+  return need + ((2 - need) & 3);
 }
 // Bytes of one block's coding scratch / record buffer: 32 uint16 lane
 // counts, then 32 lane regions (the record is compacted in place).
@@ -27,13 +29,17 @@ constexpr int64_t kRansEncTableBytes = 256 * 8 + 256 * 2;
 constexpr int64_t kRansDecTableBytes = 4096 * 4;
 
 // Dynamic shared memory of the RANS tile kernels for tiles of T blocks of B.
+//   sender:   meta, the tile's exponents (T*B), one coding buffer per block
+//   receiver: meta, the tile's sign+mantissa bytes (T*B), its records when
+//             they fit in T*B bytes (larger ones are decoded from global
+//             memory)
 constexpr int64_t kRansEncMeta = 4096;  // coder table, histogram, sizes (ciera_rans.cu)
-constexpr int64_t kRansDecMeta = 1024;  // offsets, reductions
+constexpr int64_t kRansDecMeta = 1024;  // offsets
 __host__ __device__ inline int64_t rans_compress_smem(int64_t T, int64_t B) {
-  return kRansEncMeta + 3 * T * B + T * rans_block_bytes(B);
+  return kRansEncMeta + T * B + T * rans_block_bytes(B);
 }
 __host__ __device__ inline int64_t rans_decompress_smem(int64_t T, int64_t B) {
-  return kRansDecMeta + kRansDecTableBytes + 2 * T * B + T * rans_block_bytes(B);
+  return kRansDecMeta + 2 * T * B;
 }
 
 // Launchers (ciera_rans.cu), returning a cudaError_t value.

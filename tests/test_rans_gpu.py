@@ -216,3 +216,30 @@ def test_rans_payload_needs_the_rans_flag():
     assert any(x["mode"] == ciera.MODE_RANS for x in ag.descriptors())
     ag.plan.decompress(ag.payloads, ag.descs, ag.recv_cache, ag.out, ag.workspace, rans=False)
     assert ag.status() == ciera.E_CORRUPT
+
+
+def test_rans_tile_records_larger_than_staging():
+    """A tile whose records exceed one byte per value (high-entropy changed
+    exponents) is decoded from global memory instead of shared memory."""
+    n, R, B = 4 * 65536, 4, 4096
+    rng = np.random.default_rng(23)
+    w0 = rng.integers(0, 1 << 16, n, dtype=np.uint16)
+    w1 = w0.copy()
+    S = n // R
+    for r in range(R):
+        w1[r * S:r * S + 2 * B] = rng.integers(0, 1 << 16, 2 * B, dtype=np.uint16)
+    w2 = w1.copy()
+    w2[3 * B:4 * B] ^= np.uint16(0x0080)        # one block of tile 1, rank 0
+    ag, modes = run_rans_parity([w0, w1, w2], R, B, tag="big-records")
+    assert ciera.MODE_RANS in modes
+    # the oracle's payload of iteration 1 had > T*B record bytes in tile 0
+    ref = OracleRans(n, R, B)
+    ref.step(w0)
+    res, _ = ref.step(w1)
+    pay, _, d = res[0]
+    assert int(d["mode"]) == ciera.MODE_RANS
+    nb = S // B
+    A = S
+    C = (A + (nb + 7) // 8 + 15) // 16 * 16
+    offs = pay[C + 512:C + 512 + 4 * (nb + 1)].view(np.uint32)
+    assert int(offs[2]) - int(offs[0]) > 2 * B
