@@ -144,26 +144,36 @@ __device__ __forceinline__ void flaggers_sync() {
 // bf16 field arithmetic on packed words (two values per 32-bit word).
 // exponent e = (w >> 7) & 0xFF; sign+mantissa byte s = sign << 7 | mantissa.
 
-// Exponents of the 4 values in words a (values 0,1) and b (values 2,3).
+// Exponents of the 4 values in words a (values 0,1) and b (values 2,3), one
+// per byte: bits 7..14 of each value are bytes 0 and 2 of the word >> 7.
 __device__ __forceinline__ uint32_t exp4(uint32_t a, uint32_t b) {
-  const uint32_t ea = ((a >> 7) & 0xFFu) | ((a >> 15) & 0xFF00u);
-  const uint32_t eb = ((b >> 7) & 0xFFu) | ((b >> 15) & 0xFF00u);
-  return ea | (eb << 16);
+  return __byte_perm(a >> 7, b >> 7, 0x6420);
 }
 
-// Sign+mantissa bytes of the two values of word a.
-__device__ __forceinline__ uint32_t sm2(uint32_t a) {
-  return ((a >> 8) & 0x80u) | (a & 0x7Fu) | ((a >> 16) & 0x8000u) | ((a >> 8) & 0x7F00u);
+// Sign+mantissa bytes of the two values of word a in bytes 0 and 2.
+__device__ __forceinline__ uint32_t sm_pair(uint32_t a) {
+  return ((a >> 8) & 0x00800080u) | (a & 0x007F007Fu);
 }
 
-__device__ __forceinline__ uint32_t sm4(uint32_t a, uint32_t b) { return sm2(a) | (sm2(b) << 16); }
+// Sign+mantissa bytes of the two values of word a (low 16 bits).
+__device__ __forceinline__ uint32_t sm2(uint32_t a) { return __byte_perm(sm_pair(a), 0u, 0x4420); }
+
+__device__ __forceinline__ uint32_t sm4(uint32_t a, uint32_t b) {
+  return __byte_perm(sm_pair(a), sm_pair(b), 0x6420);
+}
+
+// Four values from four sign+mantissa bytes s and four exponents e: the high
+// byte of a value is sign | exponent >> 1, the low byte exponent bit 0 <<
+// 7 | mantissa.  Returns values 0,1 in .x and 2,3 in .y.
+__device__ __forceinline__ uint2 join4(uint32_t s, uint32_t e) {
+  const uint32_t hi = (s & 0x80808080u) | ((e >> 1) & 0x7F7F7F7Fu);
+  const uint32_t lo = ((e << 7) & 0x80808080u) | (s & 0x7F7F7F7Fu);
+  return make_uint2(__byte_perm(lo, hi, 0x5140), __byte_perm(lo, hi, 0x7362));
+}
 
 // Two values from two sign+mantissa bytes (s, low 16 bits) and two exponents
 // (e, low 16 bits).
-__device__ __forceinline__ uint32_t join2(uint32_t s, uint32_t e) {
-  return ((s & 0x80u) << 8) | ((e & 0xFFu) << 7) | (s & 0x7Fu) | ((s & 0x8000u) << 16) |
-         ((e & 0xFF00u) << 15) | ((s & 0x7F00u) << 8);
-}
+__device__ __forceinline__ uint32_t join2(uint32_t s, uint32_t e) { return join4(s, e).x; }
 
 __device__ __forceinline__ uint32_t exp1(uint32_t v) { return (v >> 7) & 0xFFu; }
 __device__ __forceinline__ uint32_t sm1(uint32_t v) { return ((v >> 8) & 0x80u) | (v & 0x7Fu); }

@@ -771,12 +771,10 @@ __device__ void decompress_tile_staged(const DecompressParams& p, const Tile& x,
     } else {
       const uint4 s = reinterpret_cast<const uint4*>(ss)[gi];
       const uint4 e = reinterpret_cast<const uint4*>(cs)[gi];
-      reinterpret_cast<uint4*>(ws)[2 * gi] =
-          make_uint4(join2(s.x, e.x), join2(s.x >> 16, e.x >> 16), join2(s.y, e.y),
-                     join2(s.y >> 16, e.y >> 16));
-      reinterpret_cast<uint4*>(ws)[2 * gi + 1] =
-          make_uint4(join2(s.z, e.z), join2(s.z >> 16, e.z >> 16), join2(s.w, e.w),
-                     join2(s.w >> 16, e.w >> 16));
+      const uint2 v0 = join4(s.x, e.x), v1 = join4(s.y, e.y);
+      const uint2 v2 = join4(s.z, e.z), v3 = join4(s.w, e.w);
+      reinterpret_cast<uint4*>(ws)[2 * gi] = make_uint4(v0.x, v0.y, v1.x, v1.y);
+      reinterpret_cast<uint4*>(ws)[2 * gi + 1] = make_uint4(v2.x, v2.y, v3.x, v3.y);
     }
   }
   fence_proxy_async_smem();

@@ -183,10 +183,12 @@ __device__ uint32_t rans_encode_block(const uint8_t* exps, int L,
       const uint32_t cm = (hi >> 12) & 0xFFFu;
       const uint32_t s2 = (hi >> 24) & 0xFu;
       const uint32_t s1 = hi >> 28;
-      if (x >= ((kRansTotal - cm) << 20)) {  // x >= f * 2^20: emit the low 16 bits
-        region[--top] = static_cast<uint16_t>(x & 0xFFFFu);
-        x >>= 16;
-      }
+      // x >= f * 2^20: emit the low 16 bits.  The store is unconditional (a
+      // word not emitted is overwritten by the next one); only top moves.
+      const bool emit = x >= ((kRansTotal - cm) << 20);
+      region[top - 1] = static_cast<uint16_t>(x & 0xFFFFu);
+      top -= emit ? 1 : 0;
+      x = emit ? x >> 16 : x;
       const uint32_t t = __umulhi(x, m);
       const uint32_t q = (t + ((x - t) >> s1)) >> s2;  // floor(x / f)
       x += q * cm + c;                                 // (q << 12) + x - q f + c
@@ -231,6 +233,24 @@ __device__ uint32_t rans_encode_block(const uint8_t* exps, int L,
   return padded / 8u;
 }
 
+// One decoding step of a lane: symbol from the slot table, value and
+// exponent out, state update, and a renormalisation that reads the word
+// loaded one step ahead (branch-free; the index is clamped to the lane's
+// last word, an overrun shows in the final check).
+__device__ __forceinline__ void decode_step(const uint32_t* __restrict__ tab, const uint16_t* s,
+                                            uint32_t last, const uint8_t* sp, uint16_t* op,
+                                            uint8_t* rp, uint32_t& x, uint32_t& idx,
+                                            uint32_t& nxt) {
+  const uint32_t e = __ldg(tab + (x & (kRansTotal - 1)));
+  *op = static_cast<uint16_t>(join1(*sp, e & 0xFFu));
+  *rp = static_cast<uint8_t>(e);
+  x = ((e >> 8) & 0xFFFu) * (x >> kRansBits) + (e >> 20);
+  const bool renorm = x < kRansLow;
+  x = renorm ? (x << 16) | nxt : x;
+  idx += renorm ? 1u : 0u;
+  nxt = s[idx < last ? idx : last];
+}
+
 // One warp decodes one record of `rec_words` words into the block's L
 // exponents with the slot table `tab` (entry: symbol | f << 8 | (slot - cum)
 // << 20, read through L1), and writes each value (joined with its
@@ -248,30 +268,33 @@ __device__ bool rans_decode_block(const uint16_t* rec, uint32_t rec_words, int L
   }
   const uint32_t pre = incl - nw;
   const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
-  bool bad = rec_words < kRansLanes || kRansLanes + total > rec_words || nw < 2;
+  const bool bad = rec_words < kRansLanes || kRansLanes + total > rec_words || nw < 2;
   if (__any_sync(0xffffffffu, bad)) return false;
   const uint16_t* s = rec + kRansLanes + pre;
+  const uint32_t last = nw - 1;
   uint32_t x = (static_cast<uint32_t>(s[0]) << 16) | s[1];
   uint32_t idx = 2;
-  uint32_t nxt = idx < nw ? s[idx] : 0u;  // the next renormalisation word, loaded ahead
-  for (int j = lane; j < L; j += kRansLanes) {
-    const uint32_t e = __ldg(tab + (x & (kRansTotal - 1)));
-    const uint32_t sym = e & 0xFFu;
-    out[j] = static_cast<uint16_t>(join1(ss[j], sym));
-    rc[j] = static_cast<uint8_t>(sym);
-    x = ((e >> 8) & 0xFFFu) * (x >> kRansBits) + (e >> 20);
-    if (x < kRansLow) {
-      if (idx >= nw) {
-        bad = true;
-        break;
-      }
-      x = (x << 16) | nxt;
-      ++idx;
-      nxt = idx < nw ? s[idx] : 0u;
-    }
+  uint32_t nxt = s[idx < last ? idx : last];
+  const int n = L > lane ? (L - lane + kRansLanes - 1) / kRansLanes : 0;  // this lane's symbols
+  const uint8_t* sp = ss + lane;
+  uint16_t* op = out + lane;
+  uint8_t* rp = rc + lane;
+  int m = 0;
+  for (; m + 4 <= n; m += 4) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      decode_step(tab, s, last, sp + 32 * k, op + 32 * k, rp + 32 * k, x, idx, nxt);
+    sp += 128;
+    op += 128;
+    rp += 128;
   }
-  bad = bad || idx != nw || x != kRansLow;
-  return !__any_sync(0xffffffffu, bad);
+  for (; m < n; ++m) {
+    decode_step(tab, s, last, sp, op, rp, x, idx, nxt);
+    sp += 32;
+    op += 32;
+    rp += 32;
+  }
+  return !__any_sync(0xffffffffu, idx != nw || x != kRansLow);
 }
 
 struct RansShared {
@@ -672,10 +695,10 @@ __global__ void __launch_bounds__(kThreads)
       const uint4 e = gi0 == 0 ? kept[q] : reinterpret_cast<const uint4*>(rc)[gi];
       const uint4 s = reinterpret_cast<const uint4*>(ss)[gi];
       uint4* o = reinterpret_cast<uint4*>(out) + 2 * gi;
-      o[0] = make_uint4(join2(s.x, e.x), join2(s.x >> 16, e.x >> 16), join2(s.y, e.y),
-                        join2(s.y >> 16, e.y >> 16));
-      o[1] = make_uint4(join2(s.z, e.z), join2(s.z >> 16, e.z >> 16), join2(s.w, e.w),
-                        join2(s.w >> 16, e.w >> 16));
+      const uint2 v0 = join4(s.x, e.x), v1 = join4(s.y, e.y);
+      const uint2 v2 = join4(s.z, e.z), v3 = join4(s.w, e.w);
+      o[0] = make_uint4(v0.x, v0.y, v1.x, v1.y);
+      o[1] = make_uint4(v2.x, v2.y, v3.x, v3.y);
     }
   }
   // decode the changed blocks straight into the output and the ExpCache:
