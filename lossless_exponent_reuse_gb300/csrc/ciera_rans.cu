@@ -60,13 +60,13 @@ constexpr uint32_t kRansLow = 1u << 16;
 constexpr int kTableThreads = 256;
 
 // ---- shared-memory meta region of k_compress_rans (bytes) ----------------
-constexpr int kCTab = 0;         // uint64[256] coder entries, then uint16[256] frequencies
-constexpr int kCFreq = 2048;
-constexpr int kCHist = 2560;     // uint32[256] exponent histogram of the tile
-constexpr int kCSize = 3584;     // uint32[32] record size of each block, 16-byte units
-constexpr int kCPre = 3712;      // uint32[33] exclusive prefix of the sizes
-constexpr int kCRed = 3856;      // uint32[8] reductions
-constexpr int kCFw = 3920;       // uint32 flag bits of the tile (T <= 32)
+constexpr int kCTab = 0;         // uint4[256] coder entries, then uint16[256] frequencies
+constexpr int kCFreq = 4096;
+constexpr int kCHist = 4608;     // uint32[256] sampled exponent histogram of the tile
+constexpr int kCSize = 5632;     // uint32[32] record size of each block, 16-byte units
+constexpr int kCPre = 5760;      // uint32[33] exclusive prefix of the sizes
+constexpr int kCRed = 5904;      // uint32[8] reductions
+constexpr int kCFw = 5936;       // uint32 flag bits of the tile (T <= 32)
 static_assert(kCFw + 4 <= kRansEncMeta, "meta region");
 static_assert(kCFreq - kCTab + 512 == kRansEncTableBytes, "coder table layout");
 // ---- k_decompress_rans ---------------------------------------------------
@@ -74,20 +74,19 @@ constexpr int kDOffs = 0;        // uint32[33] record-byte prefixes of the tile'
 static_assert(kDOffs + 4 * 33 <= kRansDecMeta, "meta region");
 
 // Coder entry of a symbol of frequency f and cumulative frequency c:
-//   bits  0..31  m, the multiplier of floor(x / f) = (t + ((x - t) >> s1)) >> s2,
-//                t = mulhi(x, m), l = ceil(log2 f), m = floor(2^32 (2^l - f) / f) + 1,
-//                s1 = min(l, 1), s2 = max(l - 1, 0)
-//   bits 32..43  c
-//   bits 44..55  4096 - f
-//   bits 56..59  s2,  bit 60  s1
-__device__ __forceinline__ unsigned long long coder_entry(uint32_t f, uint32_t c) {
+//   .x  m, the multiplier of floor(x / f) = (t + ((x - t) >> s1)) >> s2 with
+//       t = mulhi(x, m), l = ceil(log2 f), m = floor(2^32 (2^l - f) / f) + 1,
+//       s1 = min(l, 1), s2 = max(l - 1, 0)
+//   .y  f * 2^20, the bound at which the state emits 16 bits first
+//   .z  4096 - f
+//   .w  c | s1 << 16 | s2 << 24
+__device__ __forceinline__ uint4 coder_entry(uint32_t f, uint32_t c) {
   const uint32_t l = 32u - __clz(f - 1u);  // ceil(log2 f); 0 for f = 1
   const unsigned long long num = (1ull << 32) * ((1ull << l) - f);
   const uint32_t m = static_cast<uint32_t>(num / f + 1ull);
   const uint32_t s1 = l < 1u ? l : 1u;
   const uint32_t s2 = l > 1u ? l - 1u : 0u;
-  const uint32_t hi = c | ((kRansTotal - f) << 12) | (s2 << 24) | (s1 << 28);
-  return (static_cast<unsigned long long>(hi) << 32) | m;
+  return make_uint4(m, f << 20, kRansTotal - f, c | (s1 << 16) | (s2 << 24));
 }
 
 // Block-wide reductions over the 256 threads of a table kernel.
@@ -156,81 +155,68 @@ __global__ void __launch_bounds__(kTableThreads)
   }
   const uint32_t c = table_exclusive_scan(f, red);
   uint8_t* t = tables + kRansEncTableBytes * static_cast<int64_t>(blockIdx.x);
-  reinterpret_cast<unsigned long long*>(t)[s] = coder_entry(f, c);
-  reinterpret_cast<uint16_t*>(t + 2048)[s] = static_cast<uint16_t>(f);
+  reinterpret_cast<uint4*>(t)[s] = coder_entry(f, c);
+  reinterpret_cast<uint16_t*>(t + kCFreq)[s] = static_cast<uint16_t>(f);
 }
 
-// One warp codes one block of L values (their exponents) into `rec`: lane
-// counts at rec[0..31], lane regions of LW words from rec[32]; then the
-// streams are compacted in place behind the counts and padded to 16 bytes.
-// Returns the record size in 16-byte units.
-__device__ uint32_t rans_encode_block(const uint8_t* exps, int L,
-                                      const unsigned long long* tab, uint16_t* rec, int LW,
-                                      int lane) {
-  uint16_t* region = rec + kRansLanes + lane * LW;
+// One warp codes one block of L exponents into its coding buffer `buf`
+// (layout: rans_block_bytes): lane l codes positions l, l+32, ... backwards,
+// emitting renormalisation words downwards from the end of its region, then
+// the final state; the lane word counts and their exclusive prefixes go to
+// the buffer's head.  Returns the record's size in 16-byte units (counts,
+// streams, zero padding); the record itself is assembled from the buffer
+// when it is stored.
+__device__ uint32_t rans_encode_block(const uint8_t* exps, int L, const uint4* tab,
+                                      uint8_t* buf, int LW, int lane) {
+  uint16_t* region = reinterpret_cast<uint16_t*>(buf + kRansBufHead) + lane * LW;
   int top = LW;
   uint32_t x = kRansLow;
-  if (lane < L) {
-    int j = lane + ((L - 1 - lane) / kRansLanes) * kRansLanes;
-    unsigned long long E = tab[exps[j]];
-    for (;;) {
-      // the next symbol's entry is loaded while this one is coded
-      const int jn = j - kRansLanes;
-      const unsigned long long En = jn >= 0 ? tab[exps[jn]] : 0ull;
-      const uint32_t m = static_cast<uint32_t>(E);
-      const uint32_t hi = static_cast<uint32_t>(E >> 32);
-      const uint32_t c = hi & 0xFFFu;
-      const uint32_t cm = (hi >> 12) & 0xFFFu;
-      const uint32_t s2 = (hi >> 24) & 0xFu;
-      const uint32_t s1 = hi >> 28;
-      // x >= f * 2^20: emit the low 16 bits.  The store is unconditional (a
-      // word not emitted is overwritten by the next one); only top moves.
-      const bool emit = x >= ((kRansTotal - cm) << 20);
-      region[top - 1] = static_cast<uint16_t>(x & 0xFFFFu);
-      top -= emit ? 1 : 0;
-      x = emit ? x >> 16 : x;
-      const uint32_t t = __umulhi(x, m);
-      const uint32_t q = (t + ((x - t) >> s1)) >> s2;  // floor(x / f)
-      x += q * cm + c;                                 // (q << 12) + x - q f + c
-      if (jn < 0) break;
-      j = jn;
-      E = En;
-    }
+  const int n = L > lane ? (L - lane + kRansLanes - 1) / kRansLanes : 0;  // this lane's symbols
+#pragma unroll 4
+  for (int m = n - 1; m >= 0; --m) {
+    const uint4 E = tab[exps[lane + kRansLanes * m]];
+    // x >= f * 2^20: emit the low 16 bits.  The store is unconditional (a
+    // word not emitted is overwritten by the next one); only top moves.
+    const bool emit = x >= E.y;
+    region[top - 1] = static_cast<uint16_t>(x & 0xFFFFu);
+    top -= emit ? 1 : 0;
+    x = emit ? x >> 16 : x;
+    const uint32_t t = __umulhi(x, E.x);
+    const uint32_t q = (t + ((x - t) >> ((E.w >> 16) & 0xFFu))) >> (E.w >> 24);  // floor(x / f)
+    x += q * E.z + (E.w & 0xFFFFu);  // (q << 12) + x - q f + c
   }
   region[--top] = static_cast<uint16_t>(x & 0xFFFFu);
   region[--top] = static_cast<uint16_t>(x >> 16);
   const uint32_t nw = static_cast<uint32_t>(LW - top);
-  rec[lane] = static_cast<uint16_t>(nw);
   uint32_t incl = nw;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += u;
   }
-  const uint32_t pre = incl - nw;
+  uint16_t* head = reinterpret_cast<uint16_t*>(buf);
+  head[lane] = static_cast<uint16_t>(nw);
+  head[kRansLanes + lane] = static_cast<uint16_t>(incl - nw);
   const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
-  __syncwarp();
-  // lane l's words move from its region's tail to 32 + prefix(l): never to a
-  // higher index, and never over a later lane's words
-  for (int l = 0; l < kRansLanes; ++l) {
-    const uint32_t n = __shfl_sync(0xffffffffu, nw, l);
-    const uint32_t p0 = __shfl_sync(0xffffffffu, pre, l);
-    const int src = kRansLanes + l * LW + (LW - static_cast<int>(n));
-    const int dst = kRansLanes + static_cast<int>(p0);
-    for (uint32_t c = 0; c < n; c += 32) {
-      const bool ok = c + lane < n;
-      uint16_t v = 0;
-      if (ok) v = rec[src + c + lane];
-      __syncwarp();
-      if (ok) rec[dst + c + lane] = v;
-      __syncwarp();
-    }
-  }
-  const uint32_t words = kRansLanes + total;
-  const uint32_t padded = (words + 7u) & ~7u;
-  if (words + lane < padded) rec[words + lane] = 0;
-  __syncwarp();
-  return padded / 8u;
+  if (lane == 31) head[2 * kRansLanes] = static_cast<uint16_t>(total);
+  return (kRansLanes + total + 7u) / 8u;
+}
+
+// Word o of the record held in coding buffer `buf`: a lane count, a stream
+// word (lane l's stream, in decoding order, is the top of its region), or
+// zero padding.
+__device__ __forceinline__ uint32_t record_word(const uint8_t* buf, int LW, uint32_t o) {
+  const uint16_t* head = reinterpret_cast<const uint16_t*>(buf);
+  if (o < kRansLanes) return head[o];
+  const uint32_t s = o - kRansLanes;
+  const uint16_t* pre = head + kRansLanes;
+  if (s >= pre[kRansLanes]) return 0u;
+  uint32_t l = 0;  // the lane whose stream holds s: largest l with pre[l] <= s
+#pragma unroll
+  for (uint32_t step = 16; step > 0; step >>= 1)
+    if (pre[l + step] <= s) l += step;
+  const uint16_t* region = reinterpret_cast<const uint16_t*>(buf + kRansBufHead);
+  return region[(l + 1) * LW - pre[l + 1] + s];
 }
 
 // One decoding step of a lane: symbol from the slot table, value and
@@ -315,7 +301,7 @@ __global__ void __launch_bounds__(kThreads)
   const int64_t B = p.geo.B;
   const int64_t T = p.geo.T;
   const int64_t TE = T * B;
-  const unsigned long long* tab = reinterpret_cast<const unsigned long long*>(dsm + kCTab);
+  const uint4* tab = reinterpret_cast<const uint4*>(dsm + kCTab);
   const uint16_t* freq = reinterpret_cast<const uint16_t*>(dsm + kCFreq);
   uint32_t* hist = reinterpret_cast<uint32_t*>(dsm + kCHist);
   uint32_t* rsize = reinterpret_cast<uint32_t*>(dsm + kCSize);
@@ -442,8 +428,7 @@ __global__ void __launch_bounds__(kThreads)
         if (i % (kThreads / 32 - 1) == warp - 1) {
           const int L = static_cast<int>((kb + 1) * B < x.te ? B : x.te - kb * B);
           const uint32_t units =
-              rans_encode_block(es + kb * B, L, tab, reinterpret_cast<uint16_t*>(scr + kb * BB),
-                                static_cast<int>(LW), lane);
+              rans_encode_block(es + kb * B, L, tab, scr + kb * BB, static_cast<int>(LW), lane);
           if (lane == 0) rsize[kb] = units;
         }
         ++i;
@@ -466,19 +451,30 @@ __global__ void __launch_bounds__(kThreads)
       if (!direct_raw && !skip)
         publish(p, x, sh.epoch, x.t == 0 ? kStateInclusive : kStateAggregate, run);
     }
-    fence_proxy_async_smem();
   }
   __syncthreads();
   if (tid == 0 && x.t > 0 && !direct_raw) publish(p, x, sh.epoch, kStateInclusive, sh.X + sh.agg);
 
   const int64_t limit = 2 * x.len;  // a payload this large goes out raw instead
-  if (tid == 0 && !direct_raw) {
-    for (int kb = 0; kb < x.nblk; ++kb) {
-      const int64_t at = Ly.D + 16 * static_cast<int64_t>(sh.X + rpre[kb]);
-      if (rsize[kb] && at + 16 * static_cast<int64_t>(rsize[kb]) <= limit)
-        bulk_s2g(payload + at, scr + kb * BB, 16u * rsize[kb]);
+  // The tile's records are one contiguous run of 16-byte units at D + 16 X:
+  // every thread assembles 32-bit words of it from the coding buffers
+  // (block by a search over the size prefixes, stream word by a search over
+  // the block's lane prefixes) and stores them coalesced.  Records that
+  // would end past 2*len are not stored: the shard then goes out raw.
+  if (!direct_raw && Ly.D + 16 * (static_cast<int64_t>(sh.X) + sh.agg) <= limit) {
+    uint32_t* dst = reinterpret_cast<uint32_t*>(payload + Ly.D) + 4 * static_cast<int64_t>(sh.X);
+    const uint32_t words32 = 4u * sh.agg;
+    const int nb1 = x.nblk;
+    for (uint32_t P = tid; P < words32; P += blockDim.x) {
+      const uint32_t unit = P >> 2;
+      int kb = 0;  // largest kb with rpre[kb] <= unit
+      for (int step = 16; step > 0; step >>= 1)
+        if (kb + step < nb1 && rpre[kb + step] <= unit) kb += step;
+      const uint8_t* buf = scr + kb * BB;
+      const uint32_t o = 2u * (P - 4u * rpre[kb]);  // first uint16 word within the record
+      dst[P] = record_word(buf, static_cast<int>(LW), o) |
+               (record_word(buf, static_cast<int>(LW), o + 1) << 16);
     }
-    bulk_commit();
   }
   if (!direct_raw) {
     uint32_t* O = reinterpret_cast<uint32_t*>(payload + Ly.O);
@@ -548,7 +544,6 @@ __global__ void __launch_bounds__(kThreads)
       p.descs[x.rl] = d;
     }
   }
-  if (tid == 0 && !direct_raw) bulk_wait_read_all();
 }
 
 // A shard that went raw only at the end (its RANS payload would not have

@@ -15,17 +15,20 @@ __host__ __device__ inline int64_t rans_lane_words(int64_t B) {
   const int64_t need = 2 + (B + kRansLanes - 1) / kRansLanes;
   return need + ((2 - need) & 3);
 }
-// Bytes of one block's coding scratch / record buffer: 32 uint16 lane
-// counts, then 32 lane regions (the record is compacted in place).
+// Bytes of one block's coding buffer: 32 uint16 lane word counts, their
+// 33 uint16 exclusive prefixes (padded to 80 bytes), then 32 lane regions
+// of rans_lane_words(B) uint16 each.
+constexpr int64_t kRansBufHead = 64 + 80;
 __host__ __device__ inline int64_t rans_block_bytes(int64_t B) {
-  return 2 * (kRansLanes + kRansLanes * rans_lane_words(B));
+  return kRansBufHead + 2 * kRansLanes * rans_lane_words(B);
 }
 
 // Per-rank coder tables in the workspace.
-//   encoder: 256 packed uint64 entries (division constants, cumulative
-//            frequency, complement), then the 256 uint16 frequencies
+//   encoder: 256 entries of 4 uint32 (division constants, renormalisation
+//            bound, complement, cumulative frequency), then the 256 uint16
+//            frequencies
 //   decoder: 4096 uint32 slot entries (symbol, frequency, slot bias)
-constexpr int64_t kRansEncTableBytes = 256 * 8 + 256 * 2;
+constexpr int64_t kRansEncTableBytes = 256 * 16 + 256 * 2;
 constexpr int64_t kRansDecTableBytes = 4096 * 4;
 
 // Dynamic shared memory of the RANS tile kernels for tiles of T blocks of B.
@@ -33,7 +36,7 @@ constexpr int64_t kRansDecTableBytes = 4096 * 4;
 //   receiver: meta, the tile's sign+mantissa bytes (T*B), its records when
 //             they fit in T*B bytes (larger ones are decoded from global
 //             memory)
-constexpr int64_t kRansEncMeta = 4096;  // coder table, histogram, sizes (ciera_rans.cu)
+constexpr int64_t kRansEncMeta = 6144;  // coder table, histogram, sizes (ciera_rans.cu)
 constexpr int64_t kRansDecMeta = 1024;  // offsets
 __host__ __device__ inline int64_t rans_compress_smem(int64_t T, int64_t B) {
   return kRansEncMeta + T * B + T * rans_block_bytes(B);
