@@ -603,8 +603,9 @@ __global__ void __launch_bounds__(kThreads)
   const int64_t B = p.geo.B;
   const int64_t T = p.geo.T;
   const int64_t TE = T * B;
+  const int nthreads = static_cast<int>(blockDim.x);  // rans_decompress_threads(T)
   if (dynamic_smem_size() < static_cast<uint32_t>(rans_decompress_smem(T, B)) || T > 32 ||
-      !p.fast) {
+      !p.fast || nthreads != rans_decompress_threads(T)) {
     if (tid == 0) atomicOr(&p.ctl->status, kStatusInternal);
     return;
   }
@@ -671,7 +672,7 @@ __global__ void __launch_bounds__(kThreads)
   uint4 kept[kPer];
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
-    const int gi = tid + q * kThreads;
+    const int gi = tid + q * nthreads;
     if (gi < ngroups && !((fw >> __umulhi(static_cast<uint32_t>(gi), mG)) & 1u))
       kept[q] = reinterpret_cast<const uint4*>(rc)[gi];
   }
@@ -682,10 +683,10 @@ __global__ void __launch_bounds__(kThreads)
     return;
   }
   // merge of the kept blocks: sign+mantissa bytes with cached exponents
-  for (int gi0 = 0; gi0 < ngroups; gi0 += kPer * kThreads) {
+  for (int gi0 = 0; gi0 < ngroups; gi0 += kPer * nthreads) {
 #pragma unroll
     for (int q = 0; q < kPer; ++q) {
-      const int gi = gi0 + tid + q * kThreads;
+      const int gi = gi0 + tid + q * nthreads;
       if (gi >= ngroups || ((fw >> __umulhi(static_cast<uint32_t>(gi), mG)) & 1u)) continue;
       const uint4 e = gi0 == 0 ? kept[q] : reinterpret_cast<const uint4*>(rc)[gi];
       const uint4 s = reinterpret_cast<const uint4*>(ss)[gi];
@@ -706,7 +707,7 @@ __global__ void __launch_bounds__(kThreads)
   for (int kb = 0; kb < x.nblk; ++kb) {
     if (!((fw >> kb) & 1u)) continue;
     const uint32_t nbytes = offs[kb + 1] - offs[kb];
-    if (i % (kThreads / 32) == warp) {
+    if (i % (nthreads / 32) == warp) {
       const int L = static_cast<int>((kb + 1) * B < x.te ? B : x.te - kb * B);
       const uint8_t* rec = staged ? recs + at : payload + Ly.D + offs[kb];
       ok = rans_decode_block(reinterpret_cast<const uint16_t*>(rec), nbytes / 2, L, tab,
@@ -772,7 +773,8 @@ int launch_decompress_rans(const DecompressParams& p, uint32_t* dec_tables, void
       p, dec_tables);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k_decompress_rans<<<static_cast<unsigned>(p.geo.total_tiles), kThreads,
+  k_decompress_rans<<<static_cast<unsigned>(p.geo.total_tiles),
+                      static_cast<unsigned>(rans_decompress_threads(p.geo.T)),
                       static_cast<size_t>(smem), s>>>(p, dec_tables);
   return cudaGetLastError();
 }

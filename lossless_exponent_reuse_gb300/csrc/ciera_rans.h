@@ -44,6 +44,10 @@ __host__ __device__ inline int64_t rans_compress_smem(int64_t T, int64_t B) {
 __host__ __device__ inline int64_t rans_decompress_smem(int64_t T, int64_t B) {
   return kRansDecMeta + 2 * T * B;
 }
+// Threads of a receiver CTA.  (Two warps for tiles of two blocks, which
+// would idle no warp, were slower: more CTAs per SM leave less L1 for the
+// slot tables.)
+__host__ __device__ inline int rans_decompress_threads(int64_t) { return 128; }
 
 // Launchers (ciera_rans.cu), returning a cudaError_t value.
 //   launch_compress_rans: the RANS sender; hist_prev/hist_out hold 256
