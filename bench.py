@@ -409,17 +409,20 @@ def run_ours(args, world, rank, local):
                 h.copy_(h0)
         ag.iteration = it0
     del snaps
-    bytes_c, bytes_d, fvals = [], [], []
+    bytes_c, bytes_d, fvals, wire = [], [], [], []
     for i in range(K):
-        bc = bd = fsum = 0.0
+        bc = bd = fsum = pw = 0.0
         for li, ag in enumerate(layers):
             ag.compress(seq[i][li])
-            c_, d_, f_ = algorithmic_bytes(ag.descriptors(), n, hashed, wl.block)
+            descs = ag.descriptors()
+            c_, d_, f_ = algorithmic_bytes(descs, n, hashed, wl.block)
             bc, bd, fsum = bc + c_, bd + d_, fsum + f_
+            pw += sum(d["payload_bytes"] for d in descs)
             ag.decompress()
         bytes_c.append(bc)
         bytes_d.append(bd)
         fvals.append(fsum / L)
+        wire.append(pw / (n * L))
     torch.cuda.synchronize()
     # the receiver's critical path alone (the paper's Decmp): every layer's
     # gather-decompress again on the final payloads (it is idempotent there)
@@ -486,7 +489,9 @@ def run_ours(args, world, rank, local):
         "data": "synthetic", "config": cfg,
         "hbm": {"achieved_gbs": round(hbm_gbs, 1), "peak_gbs": peak,
                 "frac": round(hbm_gbs / peak, 4), "peak_kind": peak_kind,
-                "changed_fraction": round(statistics.mean(fvals), 4)},
+                "changed_fraction": round(statistics.mean(fvals), 4),
+                # bytes the Allgather would carry per value (2.0 = raw bf16)
+                "wire_bytes_per_value": round(statistics.mean(wire), 4)},
         "kernels_ms": ({"compress": round(mc, 4), "decompress": round(md, 4)}
                        if mc is not None else None),
         "decompress_only_ms": round(decompress_only_ms, 4),

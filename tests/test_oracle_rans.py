@@ -117,4 +117,22 @@ def test_rans_shard_round_trip(block, p_block):
             assert d["payload_bytes"] < 2 * n
             if d_exact["mode"] == oracle.RAW:
                 assert d["payload_bytes"] < d_exact["payload_bytes"]
+            # the offset table: prefixes of the record sizes, empty for kept
+            # blocks, 16-byte steps, the last entry the records' total
+            nb = flags.size
+            A = (n + 15) // 16 * 16
+            C = (A + (nb + 7) // 8 + 15) // 16 * 16
+            O = C + 512
+            D = (O + 4 * (nb + 1) + 15) // 16 * 16
+            assert d["body_bytes"] == D
+            offs = payload[O:O + 4 * (nb + 1)].view(np.uint32).astype(np.int64)
+            sizes = np.diff(offs)
+            assert offs[0] == 0 and np.all(sizes % 16 == 0)
+            np.testing.assert_array_equal(sizes > 0, flags.astype(bool))
+            assert offs[nb] == d["payload_bytes"] - D
+            # the bitmap and the frequency table
+            bits = np.unpackbits(payload[A:A + (nb + 7) // 8], bitorder="little")[:nb]
+            np.testing.assert_array_equal(bits, flags)
+            np.testing.assert_array_equal(payload[C:C + 512].view(np.uint16),
+                                          oracle.rans_table(hist))
         hist = hist_next
