@@ -498,8 +498,9 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "peak_kind": peak_kind},
-        # compress (+ the RANS raw fixup), bitmap scan, decompress (+ the RANS tiles)
-        "gpu_launches": K * L * (5 if rans else 3),
+        # exact/hashed: compress, bitmap scan, decompress; RANS: coder tables,
+        # compress, raw fixup, bitmap scan, slot tables, decompress
+        "gpu_launches": K * L * (6 if rans else 3),
         "clocks": clk,
     }
 

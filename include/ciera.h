@@ -75,7 +75,7 @@ extern "C" {
 /* ciera_compress flags */
 #define CIERA_COLD 1u            /* no previous exponents: every block changed, payload raw */
 /* ciera_decompress flags */
-#define CIERA_DECOMPRESS_RANS 1u /* also accept CIERA_MODE_RANS payloads */
+#define CIERA_DECOMPRESS_RANS 1u /* payloads of ciera_compress_rans: RAW or RANS */
 /* Test hook: the first tile of every shard never publishes its prefix, so
  * that the tiles after it run into the bounded wait (CIERA_E_TIMEOUT). */
 #define CIERA_DEBUG_SKIP_FIRST_PUBLISH 0x80000000u
@@ -220,10 +220,12 @@ int ciera_compress_rans(ciera_plan_t plan, int rank_begin, int rank_count, const
  *   descs_dev      R descriptors (device memory)
  *   recv_cache_dev N exponent bytes (ExpCache); updated in place
  *   out_dev        N bf16 outputs
- *   flags          0, or CIERA_DECOMPRESS_RANS to accept CIERA_MODE_RANS
- *                  payloads as well (then the plan must take the fast path,
- *                  N be a multiple of 16 and every pointer be 16-byte
- *                  aligned, else CIERA_E_INVAL)
+ *   flags          0: payloads of ciera_compress / ciera_compress_hashed
+ *                  (COMPRESSED or RAW); CIERA_DECOMPRESS_RANS: payloads of
+ *                  ciera_compress_rans (RANS or RAW; a COMPRESSED payload is
+ *                  then treated as corrupt), and the plan must take the fast
+ *                  path, N be a multiple of 16 and every pointer be 16-byte
+ *                  aligned, else CIERA_E_INVAL
  * A rank whose descriptor, bitmap or frequency table does not match the
  * plan is skipped (its output range is left untouched) and CIERA_E_CORRUPT
  * is recorded for ciera_status(); so is a RANS record that does not decode

@@ -388,13 +388,20 @@ int ciera_decompress(ciera_plan_t p, const uint8_t* payloads_dev, int64_t payloa
   kp.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   kp.fast = p->fast && aligned16(payloads_dev) && (payload_stride % 16 == 0) &&
             aligned16(recv_cache_dev) && aligned16(out_dev);
+  int e;
   if (flags & CIERA_DECOMPRESS_RANS) {
     if (!kp.fast || p->numel % 16 != 0) return CIERA_E_INVAL;
     kp.rans = 1;
+    // the bitmap scan alone (no tiles), then the RANS receiver, which takes
+    // the RAW ranks too
+    DecompressParams scan = kp;
+    scan.geo.total_tiles = 0;
+    e = launch_decompress(scan, 0, stream);
+    if (e == cudaSuccess)
+      e = launch_decompress_rans(kp, reinterpret_cast<uint32_t*>(ws + p->off_rdec), stream);
+  } else {
+    e = launch_decompress(kp, kp.fast ? p->smem_decompress : 0, stream);
   }
-  int e = launch_decompress(kp, kp.fast ? p->smem_decompress : 0, stream);
-  if (e == cudaSuccess && kp.rans)
-    e = launch_decompress_rans(kp, reinterpret_cast<uint32_t*>(ws + p->off_rdec), stream);
   return e == cudaSuccess ? CIERA_OK : CIERA_E_CUDA;
 }
 

@@ -38,7 +38,8 @@
 //   k_rans_dec_tables  one CTA per RANS rank: a slot -> (symbol, frequency,
 //                      bias) table of 4096 entries from the received
 //                      frequencies, so that a decoding step is one lookup.
-//   k_decompress_rans  one CTA per tile of a RANS rank: bulk copies of the
+//   k_decompress_rans  one CTA per tile of a RAW rank (bulk copy of the
+//                      values, out and ExpCache) or of a RANS rank: bulk copies of the
 //                      sign+mantissa bytes and the records; the kept blocks
 //                      merge with their cached exponents; one warp per
 //                      changed block decodes it (slot table read through
@@ -548,15 +549,18 @@ __global__ void __launch_bounds__(kThreads)
 
 // A shard that went raw only at the end (its RANS payload would not have
 // been smaller than its raw bytes): rewrite it raw.  Shards that went raw
-// from the start were written raw by k_compress_rans itself.
+// from the start were written raw by k_compress_rans itself.  A few CTAs per
+// SM walk all tiles (usually finding nothing to do).
 __global__ void __launch_bounds__(kThreads) k_rans_raw_fixup(const CompressParams p) {
-  const Tile x = decode_tile(p.geo, blockIdx.x);
-  if (p.descs[x.rl].mode != CIERA_MODE_RAW) return;
-  if (rans_layout(x.len, x.nb).D >= 2 * x.len) return;
-  const uint4* w = reinterpret_cast<const uint4*>(p.w + x.shard_off + x.e0);
-  uint4* dst = reinterpret_cast<uint4*>(p.payloads + static_cast<int64_t>(x.rl) * p.stride +
-                                        2 * x.e0);
-  for (int64_t i = threadIdx.x; i < x.te / 8; i += blockDim.x) dst[i] = w[i];
+  for (int64_t ti = blockIdx.x; ti < p.geo.total_tiles; ti += gridDim.x) {
+    const Tile x = decode_tile(p.geo, ti);
+    if (p.descs[x.rl].mode != CIERA_MODE_RAW) continue;
+    if (rans_layout(x.len, x.nb).D >= 2 * x.len) continue;
+    const uint4* w = reinterpret_cast<const uint4*>(p.w + x.shard_off + x.e0);
+    uint4* dst = reinterpret_cast<uint4*>(p.payloads + static_cast<int64_t>(x.rl) * p.stride +
+                                          2 * x.e0);
+    for (int64_t i = threadIdx.x; i < x.te / 8; i += blockDim.x) dst[i] = w[i];
+  }
 }
 
 // One CTA per rank (RANS ranks only, after the bitmap scan has validated the
@@ -599,7 +603,13 @@ __global__ void __launch_bounds__(kThreads)
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const Tile x = decode_tile(p.geo, blockIdx.x);
-  if (p.rank_state[x.rl] != kRankRans) return;
+  const uint32_t state = p.rank_state[x.rl];
+  if (state == kRankSkip) return;
+  if (state == kRankCompressed) {
+    // not a payload of the RANS sender
+    if (threadIdx.x == 0 && x.t == 0) atomicOr(&p.ctl->status, kStatusCorrupt);
+    return;
+  }
   const int64_t B = p.geo.B;
   const int64_t T = p.geo.T;
   const int64_t TE = T * B;
@@ -607,6 +617,34 @@ __global__ void __launch_bounds__(kThreads)
   if (dynamic_smem_size() < static_cast<uint32_t>(rans_decompress_smem(T, B)) || T > 32 ||
       !p.fast || nthreads != rans_decompress_threads(T)) {
     if (tid == 0) atomicOr(&p.ctl->status, kStatusInternal);
+    return;
+  }
+  if (state == kRankRaw) {
+    // the tile's values in one bulk copy, then out and the ExpCache
+    const uint32_t te2 = 2u * static_cast<uint32_t>(x.te);
+    uint8_t* vs = dsm + kRansDecMeta;  // [2 TE]
+    if (tid == 0) {
+      mbar_init(&bar, 1);
+      fence_barrier_init();
+      mbar_arrive_expect_tx(&bar, te2);
+      bulk_g2s(vs, p.payloads + static_cast<int64_t>(x.rl) * p.stride + 2 * x.e0, te2, &bar);
+    }
+    __syncthreads();
+    if (__syncthreads_or(!mbar_wait_bounded(&bar, 0, p.timeout_ns))) {
+      if (tid == 0) atomicOr(&p.ctl->status, kStatusTimeout);
+      mbar_wait_bounded(&bar, 0, p.timeout_ns);
+      __syncthreads();
+      return;
+    }
+    uint4* out = reinterpret_cast<uint4*>(p.out + x.shard_off + x.e0);
+    uint4* rc = reinterpret_cast<uint4*>(p.rcache + x.shard_off + x.e0);
+    for (int gi = tid; gi < static_cast<int>(x.te >> 4); gi += nthreads) {
+      const uint4 w0 = reinterpret_cast<const uint4*>(vs)[2 * gi];
+      const uint4 w1 = reinterpret_cast<const uint4*>(vs)[2 * gi + 1];
+      out[2 * gi] = w0;
+      out[2 * gi + 1] = w1;
+      rc[gi] = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w), exp4(w1.x, w1.y), exp4(w1.z, w1.w));
+    }
     return;
   }
   uint32_t* offs = reinterpret_cast<uint32_t*>(dsm + kDOffs);
@@ -757,7 +795,12 @@ int launch_compress_rans(const CompressParams& p, const uint32_t* hist_prev, uin
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (!(p.flags & CIERA_COLD) && p.geo.total_tiles > 0) {
-    k_rans_raw_fixup<<<static_cast<unsigned>(p.geo.total_tiles), kThreads, 0, s>>>(p);
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = p.geo.total_tiles < 4 * sms ? p.geo.total_tiles : 4 * sms;
+    k_rans_raw_fixup<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
     e = cudaGetLastError();
   }
   return e;

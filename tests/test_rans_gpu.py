@@ -243,3 +243,17 @@ def test_rans_tile_records_larger_than_staging():
     C = (A + (nb + 7) // 8 + 15) // 16 * 16
     offs = pay[C + 512:C + 512 + 4 * (nb + 1)].view(np.uint32)
     assert int(offs[2]) - int(offs[0]) > 2 * B
+
+
+def test_rans_receiver_rejects_compressed_payloads():
+    """CIERA_DECOMPRESS_RANS takes the RANS sender's modes (RANS, RAW); a
+    COMPRESSED payload of the exact sender is reported as corrupt."""
+    n, R, B = 131072, 4, 256
+    seq = rans_sequence(n, B, seed=9)[:2]
+    ag = SimulatedAllgather(n, B, R)
+    for w in seq:
+        ag.step(torch.from_numpy(w.view(np.int16)).cuda().view(torch.uint16))
+    assert ag.status() == ciera.OK
+    assert any(d["mode"] == ciera.MODE_COMPRESSED for d in ag.descriptors())
+    ag.plan.decompress(ag.payloads, ag.descs, ag.recv_cache, ag.out, ag.workspace, rans=True)
+    assert ag.status() == ciera.E_CORRUPT
