@@ -284,6 +284,41 @@ __device__ bool rans_decode_block(const uint16_t* rec, uint32_t rec_words, int L
   return !__any_sync(0xffffffffu, idx != nw || x != kRansLow);
 }
 
+// Start pulling [src, src + bytes) into L2 (both 16-byte multiples).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// One 16-value group of the sender's streaming pass (see k_compress_rans).
+__device__ __forceinline__ void stream_group(int gi, bool in, const uint4& w0, const uint4& w1,
+                                             const uint4& cc, bool cold, bool direct_raw,
+                                             uint32_t mG, uint4* c4, uint8_t* es,
+                                             uint8_t* payload, int64_t e0, uint32_t* hist,
+                                             uint32_t& mine, int lane) {
+  uint32_t sample = 0x100u + lane;
+  if (in) {
+    const uint4 e = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w), exp4(w1.x, w1.y),
+                               exp4(w1.z, w1.w));
+    const uint32_t d = (e.x ^ cc.x) | (e.y ^ cc.y) | (e.z ^ cc.z) | (e.w ^ cc.w);
+    if (d || cold) {
+      mine |= 1u << __umulhi(static_cast<uint32_t>(gi), mG);
+      c4[gi] = e;
+    }
+    reinterpret_cast<uint4*>(es)[gi] = e;
+    if (direct_raw) {
+      uint4* dst = reinterpret_cast<uint4*>(payload + 2 * e0) + 2 * gi;
+      dst[0] = w0;
+      dst[1] = w1;
+    } else {
+      reinterpret_cast<uint4*>(payload + e0)[gi] =
+          make_uint4(sm4(w0.x, w0.y), sm4(w0.z, w0.w), sm4(w1.x, w1.y), sm4(w1.z, w1.w));
+    }
+    sample = e.x & 0xFFu;
+  }
+  const uint32_t same = __match_any_sync(0xffffffffu, sample);
+  if (in && lane == __ffs(same) - 1) atomicAdd(&hist[sample], static_cast<uint32_t>(__popc(same)));
+}
+
 struct RansShared {
   uint32_t ticket;
   uint32_t epoch;  // this launch's tag of look-back and flag words
@@ -356,6 +391,9 @@ __global__ void __launch_bounds__(kThreads)
   uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
   const uint32_t te = static_cast<uint32_t>(x.te);
   if (tid == 0) {
+    // the tile's values and cached exponents on their way into L2
+    bulk_prefetch_l2(w4, 2u * te);
+    bulk_prefetch_l2(c4, te);
     // this shard's coder table (written by k_rans_enc_tables)
     mbar_init(&bar, 1);
     fence_barrier_init();
@@ -387,31 +425,14 @@ __global__ void __launch_bounds__(kThreads)
     for (int g0 = ft - lane; g0 < ngroups; g0 += kThreads - 32) {
       const int gi = g0 + lane;
       const bool in = gi < ngroups;
-      uint32_t sample = 0x100u + lane;
+      uint4 w0 = {}, w1 = {}, cc = {};
       if (in) {
-        const uint4 w0 = __ldg(w4 + 2 * gi);
-        const uint4 w1 = __ldg(w4 + 2 * gi + 1);
-        const uint4 cc = c4[gi];
-        const uint4 e = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w), exp4(w1.x, w1.y),
-                                   exp4(w1.z, w1.w));
-        const uint32_t d = (e.x ^ cc.x) | (e.y ^ cc.y) | (e.z ^ cc.z) | (e.w ^ cc.w);
-        if (d || cold) {
-          mine |= 1u << __umulhi(static_cast<uint32_t>(gi), mG);
-          c4[gi] = e;
-        }
-        reinterpret_cast<uint4*>(es)[gi] = e;
-        if (direct_raw) {
-          uint4* dst = reinterpret_cast<uint4*>(payload + 2 * x.e0) + 2 * gi;
-          dst[0] = w0;
-          dst[1] = w1;
-        } else {
-          reinterpret_cast<uint4*>(payload + x.e0)[gi] =
-              make_uint4(sm4(w0.x, w0.y), sm4(w0.z, w0.w), sm4(w1.x, w1.y), sm4(w1.z, w1.w));
-        }
-        sample = e.x & 0xFFu;
+        w0 = __ldg(w4 + 2 * gi);
+        w1 = __ldg(w4 + 2 * gi + 1);
+        cc = c4[gi];
       }
-      const uint32_t same = __match_any_sync(0xffffffffu, sample);
-      if (in && lane == __ffs(same) - 1) atomicAdd(&hist[sample], static_cast<uint32_t>(__popc(same)));
+      stream_group(gi, in, w0, w1, cc, cold, direct_raw, mG, c4, es, payload, x.e0, hist, mine,
+                   lane);
     }
     mine = __reduce_or_sync(0xffffffffu, mine);
     if (lane == 0 && mine) atomicOr(&fw[0], mine);
