@@ -423,6 +423,12 @@ def run_ours(args, world, rank, local):
         bytes_d.append(bd)
         fvals.append(fsum / L)
         wire.append(pw / (n * L))
+    # exponent change rate between consecutive timed iterations (first layer)
+    exp_rates = []
+    for i in range(1, K):
+        e0 = (seq[i - 1][0].view(torch.int16).to(torch.int32) >> 7) & 0xFF
+        e1 = (seq[i][0].view(torch.int16).to(torch.int32) >> 7) & 0xFF
+        exp_rates.append(float((e0 != e1).float().mean()))
     torch.cuda.synchronize()
     # the receiver's critical path alone (the paper's Decmp): every layer's
     # gather-decompress again on the final payloads (it is idempotent there)
@@ -491,7 +497,9 @@ def run_ours(args, world, rank, local):
                 "frac": round(hbm_gbs / peak, 4), "peak_kind": peak_kind,
                 "changed_fraction": round(statistics.mean(fvals), 4),
                 # bytes the Allgather would carry per value (2.0 = raw bf16)
-                "wire_bytes_per_value": round(statistics.mean(wire), 4)},
+                "wire_bytes_per_value": round(statistics.mean(wire), 4),
+                "exponent_change_rate": (round(statistics.mean(exp_rates), 5)
+                                         if exp_rates else None)},
         "kernels_ms": ({"compress": round(mc, 4), "decompress": round(md, 4)}
                        if mc is not None else None),
         "decompress_only_ms": round(decompress_only_ms, 4),
