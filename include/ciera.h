@@ -67,6 +67,7 @@ extern "C" {
 #define CIERA_E_CORRUPT (-3)     /* a received descriptor/bitmap does not match the plan */
 #define CIERA_E_TIMEOUT (-4)     /* a bounded device-side wait ran out */
 #define CIERA_E_INTERNAL (-5)    /* a kernel found its launch configuration inconsistent */
+#define CIERA_E_BOUNDS (-6)      /* checked builds: an access outside its buffer was skipped */
 
 #define CIERA_MODE_COMPRESSED 0u
 #define CIERA_MODE_RAW 1u
@@ -79,6 +80,11 @@ extern "C" {
 /* Test hook: the first tile of every shard never publishes its prefix, so
  * that the tiles after it run into the bounded wait (CIERA_E_TIMEOUT). */
 #define CIERA_DEBUG_SKIP_FIRST_PUBLISH 0x80000000u
+/* Test hook of checked builds only (a library built with -DCIERA_CHECKED;
+ * other builds reject the flag with CIERA_E_INVAL): ciera_compress moves
+ * its payload stores 2^40 bytes out of range, so that the bounds checks
+ * skip them and record CIERA_E_BOUNDS. */
+#define CIERA_DEBUG_OUT_OF_RANGE 0x40000000u
 
 typedef struct ciera_plan_s *ciera_plan_t;
 
@@ -236,8 +242,8 @@ int ciera_decompress(ciera_plan_t plan, const uint8_t *payloads_dev, int64_t pay
                      void *workspace_dev, uint32_t flags, void *stream);
 
 /* Wait for `stream`, then read and clear the workspace's status word.
- * Returns CIERA_OK, CIERA_E_CORRUPT, CIERA_E_TIMEOUT, CIERA_E_INTERNAL or
- * CIERA_E_CUDA. */
+ * Returns CIERA_OK, CIERA_E_CORRUPT, CIERA_E_TIMEOUT, CIERA_E_INTERNAL,
+ * CIERA_E_BOUNDS (checked builds only) or CIERA_E_CUDA. */
 int ciera_status(void *workspace_dev, void *stream);
 
 /* Sender side without a workspace, for callers that cannot allocate device

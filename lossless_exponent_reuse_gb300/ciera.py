@@ -27,6 +27,7 @@ E_CUDA = -2
 E_CORRUPT = -3
 E_TIMEOUT = -4
 E_INTERNAL = -5
+E_BOUNDS = -6
 
 MODE_COMPRESSED = 0
 MODE_RAW = 1
@@ -35,6 +36,7 @@ MODE_RANS = 2
 COLD = 1
 DECOMPRESS_RANS = 1
 DEBUG_SKIP_FIRST_PUBLISH = 0x80000000
+DEBUG_OUT_OF_RANGE = 0x40000000  # accepted by checked builds only
 
 DESC_BYTES = 24
 
@@ -99,12 +101,18 @@ _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
 
 
+def checked_build() -> bool:
+    """True when this process uses the checked build of the library
+    (environment variable CIERA_CHECKED=1, read at the first load)."""
+    return os.environ.get("CIERA_CHECKED", "") == "1"
+
+
 def lib() -> ctypes.CDLL:
     """Load libciera (building it in-tree first if it is missing or stale)."""
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.build()
+            path = _build.build(checked=checked_build())
             L = ctypes.CDLL(path)
             for name, (res, args) in SIGNATURES.items():
                 fn = getattr(L, name)
@@ -115,7 +123,7 @@ def lib() -> ctypes.CDLL:
 
 
 def library_path() -> str:
-    return _build.LIB
+    return _build.library_path(checked_build())
 
 
 def strerror(status: int) -> str:

@@ -20,6 +20,15 @@
 
 using namespace ciera;
 
+// Flags every compress entry point accepts; the out-of-range test hook only
+// in checked builds, where the kernels skip the accesses it provokes.
+#ifdef CIERA_CHECKED
+constexpr uint32_t kCompressFlags =
+    CIERA_COLD | CIERA_DEBUG_SKIP_FIRST_PUBLISH | CIERA_DEBUG_OUT_OF_RANGE;
+#else
+constexpr uint32_t kCompressFlags = CIERA_COLD | CIERA_DEBUG_SKIP_FIRST_PUBLISH;
+#endif
+
 struct ciera_plan_s {
   int64_t numel;
   int64_t ranks;
@@ -98,6 +107,7 @@ const char* ciera_strerror(int status) {
     case CIERA_E_CORRUPT: return "corrupt descriptor or bitmap";
     case CIERA_E_TIMEOUT: return "bounded device wait timed out";
     case CIERA_E_INTERNAL: return "internal launch configuration error";
+    case CIERA_E_BOUNDS: return "out-of-range access skipped (checked build)";
     default: return "unknown status";
   }
 }
@@ -197,8 +207,7 @@ int compress_impl(ciera_plan_t p, int rank_begin, int rank_count, const uint16_t
   const Geometry g = range_geometry(p, rank_begin, rank_count);
   if (g.total_tiles > 0 && (!w_dev || (hashed ? !hash_cache_dev : !sender_cache_dev)))
     return CIERA_E_INVAL;
-  const uint32_t known = CIERA_COLD | CIERA_DEBUG_SKIP_FIRST_PUBLISH;
-  if (flags & ~known) return CIERA_E_INVAL;
+  if (flags & ~kCompressFlags) return CIERA_E_INVAL;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace_dev);
   CompressParams kp{};
@@ -260,8 +269,7 @@ int ciera_compress_rans(ciera_plan_t p, int rank_begin, int rank_count, const ui
   if (!payloads_dev || !descs_dev || !workspace_dev || payload_stride < p->capacity ||
       !hist_prev_dev || !hist_out_dev)
     return CIERA_E_INVAL;
-  const uint32_t known = CIERA_COLD | CIERA_DEBUG_SKIP_FIRST_PUBLISH;
-  if (flags & ~known) return CIERA_E_INVAL;
+  if (flags & ~kCompressFlags) return CIERA_E_INVAL;
   // staged kernel only: every shard a multiple of 16 values, aligned operands
   if (!p->fast || p->numel % 16 != 0 || p->S > (int64_t(1) << 30) || p->T > 32)
     return CIERA_E_INVAL;
@@ -420,6 +428,7 @@ int ciera_status(void* workspace_dev, void* stream) {
       return CIERA_E_CUDA;
   }
   if (status & kStatusInternal) return CIERA_E_INTERNAL;
+  if (status & kStatusBounds) return CIERA_E_BOUNDS;
   if (status & kStatusTimeout) return CIERA_E_TIMEOUT;
   if (status & kStatusCorrupt) return CIERA_E_CORRUPT;
   return CIERA_OK;

@@ -135,6 +135,26 @@ __device__ __forceinline__ void record_status(Control* ctl, uint32_t bits) {
   atomicOr(&ctl->status, bits);
 }
 
+// Checked builds (-DCIERA_CHECKED): global accesses at computed offsets are
+// tested against their buffer first; one that would leave it is skipped and
+// kStatusBounds recorded (no trap, no assert).  Other builds compile the
+// test away.
+#ifdef CIERA_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
+// True if [off, off + size) lies inside [0, limit); in checked builds a
+// false result also records kStatusBounds.
+__device__ __forceinline__ bool in_bounds(Control* ctl, int64_t off, int64_t size,
+                                          int64_t limit) {
+  if (!kChecked) return true;
+  if (off >= 0 && size >= 0 && off <= limit - size) return true;
+  atomicOr(&ctl->status, kStatusBounds);
+  return false;
+}
+
 // Named barrier of the 96 worker threads (warps 1-3) of a compress CTA.
 __device__ __forceinline__ void flaggers_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 32) : "memory");

@@ -29,7 +29,12 @@ struct Control {
   uint32_t status;   // kStatus* bits, read and cleared by ciera_status
   uint32_t pad[61];
 };
-enum : uint32_t { kStatusCorrupt = 1u, kStatusTimeout = 2u, kStatusInternal = 4u };
+enum : uint32_t {
+  kStatusCorrupt = 1u,
+  kStatusTimeout = 2u,
+  kStatusInternal = 4u,
+  kStatusBounds = 8u,  // checked builds: an access outside its buffer was skipped
+};
 
 // Decoupled look-back status word of one tile (and, beside it, an
 // epoch-tagged word with the tile's flag bits):

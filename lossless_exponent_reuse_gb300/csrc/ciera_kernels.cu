@@ -203,7 +203,7 @@ __device__ void compress_epilogue(const CompressParams& p, const Tile& x, const 
         }
         byte |= ((bits >> (k - tj * T)) & 1u) << j;
       }
-      payload[body + i] = static_cast<uint8_t>(byte);
+      if (in_bounds(p.ctl, body + i, 1, p.stride)) payload[body + i] = static_cast<uint8_t>(byte);
     }
     if (to) record_status(p.ctl, kStatusTimeout);
   } else {
@@ -216,7 +216,7 @@ __device__ void compress_epilogue(const CompressParams& p, const Tile& x, const 
         const int64_t k = 8 * i + j;
         if (k < x.nb) byte |= static_cast<uint32_t>(__ldcg(fb + k) & 1u) << j;
       }
-      payload[body + i] = static_cast<uint8_t>(byte);
+      if (in_bounds(p.ctl, body + i, 1, p.stride)) payload[body + i] = static_cast<uint8_t>(byte);
     }
   }
 }
@@ -486,11 +486,11 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
         const int64_t ea = static_cast<int64_t>(ka) * B;
         const int64_t ez =
             static_cast<int64_t>(kz) * B < x.te ? static_cast<int64_t>(kz) * B : x.te;
-        const int64_t off = (x.k0 + ka + sh.X + count_before(fw, fpre, ka)) * B;
-        if (f)
-          bulk_s2g(payload + off, ws + 2 * ea, static_cast<uint32_t>(2 * (ez - ea)));
-        else
-          bulk_s2g(payload + off, cs + ea, static_cast<uint32_t>(ez - ea));
+        int64_t off = (x.k0 + ka + sh.X + count_before(fw, fpre, ka)) * B;
+        if (kChecked && (p.flags & CIERA_DEBUG_OUT_OF_RANGE)) off += int64_t(1) << 40;
+        const int64_t bytes = (f ? 2 : 1) * (ez - ea);
+        if (in_bounds(p.ctl, off, bytes, p.stride))
+          bulk_s2g(payload + off, f ? ws + 2 * ea : cs + ea, static_cast<uint32_t>(bytes));
         ka = kz;
       }
       bulk_commit();
@@ -503,13 +503,15 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
       const int64_t off = (kg + sh.X + count_before(fw, fpre, kb)) * B;
       const uint32_t v = w[j];
       if (flag_of(fw, kb)) {
-        payload[off + 2 * within] = static_cast<uint8_t>(v & 0xFFu);
-        payload[off + 2 * within + 1] = static_cast<uint8_t>(v >> 8);
+        if (in_bounds(p.ctl, off + 2 * within, 2, p.stride)) {
+          payload[off + 2 * within] = static_cast<uint8_t>(v & 0xFFu);
+          payload[off + 2 * within + 1] = static_cast<uint8_t>(v >> 8);
+        }
         if (!kHashed) {
           const uint8_t e = static_cast<uint8_t>(exp1(v));
           if (c[j] != e) c[j] = e;
         }
-      } else {
+      } else if (in_bounds(p.ctl, off + within, 1, p.stride)) {
         payload[off + within] = static_cast<uint8_t>(sm1(v));
       }
     }
@@ -525,11 +527,13 @@ __global__ void __launch_bounds__(kThreads) k_raw_fixup(const CompressParams p) 
   const ciera_desc d = p.descs[x.rl];
   if (d.mode != CIERA_MODE_RAW || d.n_changed_blocks >= x.nb) return;
   const uint16_t* w = p.w + x.shard_off + x.e0;
-  uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride + 2 * x.e0;
+  uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
   for (int64_t j = threadIdx.x; j < x.te; j += blockDim.x) {
     const uint32_t v = w[j];
-    payload[2 * j] = static_cast<uint8_t>(v & 0xFFu);
-    payload[2 * j + 1] = static_cast<uint8_t>(v >> 8);
+    const int64_t o = 2 * (x.e0 + j);
+    if (!in_bounds(p.ctl, o, 2, p.stride)) continue;
+    payload[o] = static_cast<uint8_t>(v & 0xFFu);
+    payload[o + 1] = static_cast<uint8_t>(v >> 8);
   }
 }
 
@@ -603,7 +607,8 @@ __global__ void __launch_bounds__(kScanThreads) k_bitmap_scan(const DecompressPa
       uint32_t word = 0;
       for (int j = 0; j < 4; ++j) {
         const int64_t b = 4 * i + j;
-        if (b < bm) word |= static_cast<uint32_t>(bitmap[b]) << (8 * j);
+        if (b < bm && in_bounds(p.ctl, (bitmap - payload) + b, 1, p.stride))
+          word |= static_cast<uint32_t>(bitmap[b]) << (8 * j);
       }
       if (i == nw - 1 && (nb & 31)) {
         // bits past the last block must be zero
@@ -665,6 +670,7 @@ __device__ void decompress_tile_bytes(const DecompressParams& p, const Tile& x, 
   if (state == kRankRaw) {
     for (int64_t j = threadIdx.x; j < x.te; j += blockDim.x) {
       const int64_t o = 2 * (x.e0 + j);
+      if (!in_bounds(p.ctl, o, 2, p.stride)) continue;
       const uint32_t v = payload[o] | (static_cast<uint32_t>(payload[o + 1]) << 8);
       out[j] = static_cast<uint16_t>(v);
       rc[j] = static_cast<uint8_t>(exp1(v));
@@ -682,10 +688,11 @@ __device__ void decompress_tile_bytes(const DecompressParams& p, const Tile& x, 
     const int64_t off = (kg + C) * B;
     if ((word >> bit) & 1u) {
       const int64_t o = off + 2 * within;
+      if (!in_bounds(p.ctl, o, 2, p.stride)) continue;
       const uint32_t v = payload[o] | (static_cast<uint32_t>(payload[o + 1]) << 8);
       out[j] = static_cast<uint16_t>(v);
       rc[j] = static_cast<uint8_t>(exp1(v));
-    } else {
+    } else if (in_bounds(p.ctl, off + within, 1, p.stride)) {
       out[j] = static_cast<uint16_t>(join1(payload[off + within], rc[j]));
     }
   }
@@ -712,7 +719,7 @@ __device__ void decompress_tile_staged(const DecompressParams& p, const Tile& x,
       sh.fw[0] = 0xffffffffu;
       sh.X = 0;
       mbar_arrive_expect_tx(bar, 2u * te);
-      bulk_g2s(ws, payload + 2 * x.e0, 2u * te, bar);
+      if (in_bounds(p.ctl, 2 * x.e0, 2 * te, p.stride)) bulk_g2s(ws, payload + 2 * x.e0, 2u * te, bar);
     } else {
       // flag bits of blocks k0 .. k0+nblk-1 (nblk <= 32, may straddle a word)
       const uint32_t* words = p.bm_words + static_cast<int64_t>(x.rl) * p.nw_stride;
@@ -741,10 +748,12 @@ __device__ void decompress_tile_staged(const DecompressParams& p, const Tile& x,
         const int64_t ez = static_cast<int64_t>(kz) * B < x.te ? static_cast<int64_t>(kz) * B : x.te;
         const int64_t off = (x.k0 + ka + X + before) * B;
         if (f) {
-          bulk_g2s(ws + 2 * ea, payload + off, static_cast<uint32_t>(2 * (ez - ea)), bar);
+          if (in_bounds(p.ctl, off, 2 * (ez - ea), p.stride))
+            bulk_g2s(ws + 2 * ea, payload + off, static_cast<uint32_t>(2 * (ez - ea)), bar);
           before += static_cast<uint32_t>(kz - ka);
         } else {
-          bulk_g2s(ss + ea, payload + off, static_cast<uint32_t>(ez - ea), bar);
+          if (in_bounds(p.ctl, off, ez - ea, p.stride))
+            bulk_g2s(ss + ea, payload + off, static_cast<uint32_t>(ez - ea), bar);
           bulk_g2s(cs + ea, rc + ea, static_cast<uint32_t>(ez - ea), bar);
         }
         ka = kz;

@@ -293,8 +293,9 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
 __device__ __forceinline__ void stream_group(int gi, bool in, const uint4& w0, const uint4& w1,
                                              const uint4& cc, bool cold, bool direct_raw,
                                              uint32_t mG, uint4* c4, uint8_t* es,
-                                             uint8_t* payload, int64_t e0, uint32_t* hist,
-                                             uint32_t& mine, int lane) {
+                                             uint8_t* payload, int64_t e0, int64_t stride,
+                                             Control* ctl, uint32_t* hist, uint32_t& mine,
+                                             int lane) {
   uint32_t sample = 0x100u + lane;
   if (in) {
     const uint4 e = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w), exp4(w1.x, w1.y),
@@ -306,10 +307,12 @@ __device__ __forceinline__ void stream_group(int gi, bool in, const uint4& w0, c
     }
     reinterpret_cast<uint4*>(es)[gi] = e;
     if (direct_raw) {
-      uint4* dst = reinterpret_cast<uint4*>(payload + 2 * e0) + 2 * gi;
-      dst[0] = w0;
-      dst[1] = w1;
-    } else {
+      if (in_bounds(ctl, 2 * e0 + 32 * static_cast<int64_t>(gi), 32, stride)) {
+        uint4* dst = reinterpret_cast<uint4*>(payload + 2 * e0) + 2 * gi;
+        dst[0] = w0;
+        dst[1] = w1;
+      }
+    } else if (in_bounds(ctl, e0 + 16 * static_cast<int64_t>(gi), 16, stride)) {
       reinterpret_cast<uint4*>(payload + e0)[gi] =
           make_uint4(sm4(w0.x, w0.y), sm4(w0.z, w0.w), sm4(w1.x, w1.y), sm4(w1.z, w1.w));
     }
@@ -431,8 +434,8 @@ __global__ void __launch_bounds__(kThreads)
         w1 = __ldg(w4 + 2 * gi + 1);
         cc = c4[gi];
       }
-      stream_group(gi, in, w0, w1, cc, cold, direct_raw, mG, c4, es, payload, x.e0, hist, mine,
-                   lane);
+      stream_group(gi, in, w0, w1, cc, cold, direct_raw, mG, c4, es, payload, x.e0, p.stride,
+                   p.ctl, hist, mine, lane);
     }
     mine = __reduce_or_sync(0xffffffffu, mine);
     if (lane == 0 && mine) atomicOr(&fw[0], mine);
@@ -494,14 +497,19 @@ __global__ void __launch_bounds__(kThreads)
         if (kb + step < nb1 && rpre[kb + step] <= unit) kb += step;
       const uint8_t* buf = scr + kb * BB;
       const uint32_t o = 2u * (P - 4u * rpre[kb]);  // first uint16 word within the record
+      if (!in_bounds(p.ctl, Ly.D + 16 * static_cast<int64_t>(sh.X) + 4 * static_cast<int64_t>(P),
+                     4, p.stride))
+        continue;
       dst[P] = record_word(buf, static_cast<int>(LW), o) |
                (record_word(buf, static_cast<int>(LW), o + 1) << 16);
     }
   }
   if (!direct_raw) {
     uint32_t* O = reinterpret_cast<uint32_t*>(payload + Ly.O);
-    if (tid < x.nblk) O[x.k0 + tid] = 16u * (sh.X + rpre[tid]);
-    if (tid == 0 && x.t == x.tiles - 1) O[x.nb] = 16u * (sh.X + sh.agg);
+    if (tid < x.nblk && in_bounds(p.ctl, Ly.O + 4 * (x.k0 + tid), 4, p.stride))
+      O[x.k0 + tid] = 16u * (sh.X + rpre[tid]);
+    if (tid == 0 && x.t == x.tiles - 1 && in_bounds(p.ctl, Ly.O + 4 * x.nb, 4, p.stride))
+      O[x.nb] = 16u * (sh.X + sh.agg);
   }
   uint32_t* ho = hist_out + 256 * static_cast<int64_t>(x.rl);
   for (int s = tid; s < 256; s += blockDim.x)
@@ -543,14 +551,15 @@ __global__ void __launch_bounds__(kThreads)
         byte |= ((bits >> (k - tj * T)) & 1u) << j;
       }
       nch += __popc(byte);
-      if (!raw) payload[Ly.A + i] = static_cast<uint8_t>(byte);
+      if (!raw && in_bounds(p.ctl, Ly.A + i, 1, p.stride))
+        payload[Ly.A + i] = static_cast<uint8_t>(byte);
     }
     if (to) record_status(p.ctl, kStatusTimeout);
     const uint32_t tot = warp_sum(nch);
     if (lane == 0) red[warp] = tot;
     __syncthreads();
     const uint32_t n_changed = red[0] + red[1] + red[2] + red[3];
-    if (!raw) {
+    if (!raw && in_bounds(p.ctl, 0, Ly.D, p.stride)) {
       for (int s = tid; s < 256; s += blockDim.x)
         reinterpret_cast<uint16_t*>(payload + Ly.C)[s] = freq[s];
       // zero padding before the table and before the records
@@ -580,6 +589,7 @@ __global__ void __launch_bounds__(kThreads) k_rans_raw_fixup(const CompressParam
     const uint4* w = reinterpret_cast<const uint4*>(p.w + x.shard_off + x.e0);
     uint4* dst = reinterpret_cast<uint4*>(p.payloads + static_cast<int64_t>(x.rl) * p.stride +
                                           2 * x.e0);
+    if (!in_bounds(p.ctl, 2 * x.e0, 2 * x.te, p.stride)) continue;
     for (int64_t i = threadIdx.x; i < x.te / 8; i += blockDim.x) dst[i] = w[i];
   }
 }
@@ -596,8 +606,11 @@ __global__ void __launch_bounds__(kTableThreads)
   const int s = threadIdx.x;
   const int64_t len = shard_len_of(p.geo, r);
   const int64_t nb = (len + p.geo.B - 1) / p.geo.B;
-  const uint8_t* tab = p.payloads + static_cast<int64_t>(r) * p.stride + rans_layout(len, nb).C;
-  const uint32_t f = tab[2 * s] | (static_cast<uint32_t>(tab[2 * s + 1]) << 8);
+  const int64_t C = rans_layout(len, nb).C;
+  const uint8_t* tab = p.payloads + static_cast<int64_t>(r) * p.stride + C;
+  const uint32_t f = in_bounds(p.ctl, C + 2 * s, 2, p.stride)
+                         ? tab[2 * s] | (static_cast<uint32_t>(tab[2 * s + 1]) << 8)
+                         : 16u;
   const uint32_t c = table_exclusive_scan(f, red);
   cum[s] = c;
   if (s == kTableThreads - 1) cum[256] = c + f;
@@ -648,7 +661,8 @@ __global__ void __launch_bounds__(kThreads)
       mbar_init(&bar, 1);
       fence_barrier_init();
       mbar_arrive_expect_tx(&bar, te2);
-      bulk_g2s(vs, p.payloads + static_cast<int64_t>(x.rl) * p.stride + 2 * x.e0, te2, &bar);
+      if (in_bounds(p.ctl, 2 * x.e0, te2, p.stride))
+        bulk_g2s(vs, p.payloads + static_cast<int64_t>(x.rl) * p.stride + 2 * x.e0, te2, &bar);
     }
     __syncthreads();
     if (__syncthreads_or(!mbar_wait_bounded(&bar, 0, p.timeout_ns))) {
@@ -677,7 +691,10 @@ __global__ void __launch_bounds__(kThreads)
   uint8_t* rc = p.rcache + x.shard_off + x.e0;
   uint16_t* out = p.out + x.shard_off + x.e0;
   const uint32_t te = static_cast<uint32_t>(x.te);
-  if (tid <= x.nblk) offs[tid] = reinterpret_cast<const uint32_t*>(payload + Ly.O)[x.k0 + tid];
+  if (tid <= x.nblk)
+    offs[tid] = in_bounds(p.ctl, Ly.O + 4 * (x.k0 + tid), 4, p.stride)
+                    ? reinterpret_cast<const uint32_t*>(payload + Ly.O)[x.k0 + tid]
+                    : 0u;
   __syncthreads();
   if (tid == 0) {
     // the tile's flag bits (from the aligned copy of the bitmap)
@@ -712,12 +729,13 @@ __global__ void __launch_bounds__(kThreads)
     mbar_init(&bar, 1);
     fence_barrier_init();
     mbar_arrive_expect_tx(&bar, te + (staged ? static_cast<uint32_t>(rec_bytes) : 0u));
-    bulk_g2s(ss, payload + x.e0, te, &bar);
+    if (in_bounds(p.ctl, x.e0, te, p.stride)) bulk_g2s(ss, payload + x.e0, te, &bar);
     if (staged) {
       uint32_t at = 0;
       for (int kb = 0; kb < x.nblk; ++kb)
         if ((fw >> kb) & 1u) {
-          bulk_g2s(recs + at, payload + Ly.D + offs[kb], offs[kb + 1] - offs[kb], &bar);
+          if (in_bounds(p.ctl, Ly.D + offs[kb], offs[kb + 1] - offs[kb], p.stride))
+            bulk_g2s(recs + at, payload + Ly.D + offs[kb], offs[kb + 1] - offs[kb], &bar);
           at += offs[kb + 1] - offs[kb];
         }
     }
@@ -769,7 +787,8 @@ __global__ void __launch_bounds__(kThreads)
     if (i % (nthreads / 32) == warp) {
       const int L = static_cast<int>((kb + 1) * B < x.te ? B : x.te - kb * B);
       const uint8_t* rec = staged ? recs + at : payload + Ly.D + offs[kb];
-      ok = rans_decode_block(reinterpret_cast<const uint16_t*>(rec), nbytes / 2, L, tab,
+      if (!staged && !in_bounds(p.ctl, Ly.D + offs[kb], nbytes, p.stride)) rec = nullptr;
+      ok = rec != nullptr && rans_decode_block(reinterpret_cast<const uint16_t*>(rec), nbytes / 2, L, tab,
                              ss + kb * B, out + kb * B, rc + kb * B, lane) && ok;
     }
     at += nbytes;

@@ -84,6 +84,9 @@ def test_compress_rejects_bad_ranges_without_touching_the_gpu():
     assert L.ciera_compress(*args(0, 4, cap - 1)) == ciera.E_INVAL  # short stride
     assert L.ciera_compress(p.handle, 0, 4, fake, fake, fake, cap, fake, None, fake, 0x40,
                             None) == ciera.E_INVAL                  # unknown flag
+    if not ciera.checked_build():                # the test hook of checked builds only
+        assert L.ciera_compress(p.handle, 0, 4, fake, fake, fake, cap, fake, None, fake,
+                                ciera.DEBUG_OUT_OF_RANGE, None) == ciera.E_INVAL
     assert L.ciera_decompress(p.handle, fake, cap - 1, fake, fake, fake, fake, 0,
                               None) == ciera.E_INVAL
     assert L.ciera_decompress(p.handle, fake, cap, fake, fake, fake, fake, 2,
@@ -166,3 +169,13 @@ def test_rans_entry_points_reject_what_the_staged_kernels_cannot_take():
                               ciera.DECOMPRESS_RANS, None) == ciera.E_INVAL
     assert L.ciera_decompress(p.handle, fake, p.info.payload_capacity, fake, odd, fake, fake,
                               ciera.DECOMPRESS_RANS, None) == ciera.E_INVAL
+
+
+def test_checked_build_compiles_and_exports_the_same_symbols():
+    import ctypes as ct
+    from lossless_exponent_reuse_gb300 import _build
+    path = _build.build(checked=True)
+    L = ct.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert L.ciera_strerror(ciera.E_BOUNDS) is not None
