@@ -203,23 +203,6 @@ __device__ uint32_t rans_encode_block(const uint8_t* exps, int L, const uint4* t
   return (kRansLanes + total + 7u) / 8u;
 }
 
-// Word o of the record held in coding buffer `buf`: a lane count, a stream
-// word (lane l's stream, in decoding order, is the top of its region), or
-// zero padding.
-__device__ __forceinline__ uint32_t record_word(const uint8_t* buf, int LW, uint32_t o) {
-  const uint16_t* head = reinterpret_cast<const uint16_t*>(buf);
-  if (o < kRansLanes) return head[o];
-  const uint32_t s = o - kRansLanes;
-  const uint16_t* pre = head + kRansLanes;
-  if (s >= pre[kRansLanes]) return 0u;
-  uint32_t l = 0;  // the lane whose stream holds s: largest l with pre[l] <= s
-#pragma unroll
-  for (uint32_t step = 16; step > 0; step >>= 1)
-    if (pre[l + step] <= s) l += step;
-  const uint16_t* region = reinterpret_cast<const uint16_t*>(buf + kRansBufHead);
-  return region[(l + 1) * LW - pre[l + 1] + s];
-}
-
 // One decoding step of a lane: symbol from the slot table, value and
 // exponent out, state update, and a renormalisation that reads the word
 // loaded one step ahead (branch-free; the index is clamped to the lane's
@@ -481,27 +464,30 @@ __global__ void __launch_bounds__(kThreads)
   if (tid == 0 && x.t > 0 && !direct_raw) publish(p, x, sh.epoch, kStateInclusive, sh.X + sh.agg);
 
   const int64_t limit = 2 * x.len;  // a payload this large goes out raw instead
-  // The tile's records are one contiguous run of 16-byte units at D + 16 X:
-  // every thread assembles 32-bit words of it from the coding buffers
-  // (block by a search over the size prefixes, stream word by a search over
-  // the block's lane prefixes) and stores them coalesced.  Records that
-  // would end past 2*len are not stored: the shard then goes out raw.
+  // The tile's records are one contiguous run of 16-byte units at D + 16 X.
+  // One warp per changed block stores its record: lane l writes its word
+  // count and copies its own stream (the top of its region) to its place
+  // behind the counts; the lanes below the padding write its zeros.  Records
+  // that would end past 2*len are not stored: the shard then goes out raw.
   if (!direct_raw && Ly.D + 16 * (static_cast<int64_t>(sh.X) + sh.agg) <= limit) {
-    uint32_t* dst = reinterpret_cast<uint32_t*>(payload + Ly.D) + 4 * static_cast<int64_t>(sh.X);
-    const uint32_t words32 = 4u * sh.agg;
-    const int nb1 = x.nblk;
-    for (uint32_t P = tid; P < words32; P += blockDim.x) {
-      const uint32_t unit = P >> 2;
-      int kb = 0;  // largest kb with rpre[kb] <= unit
-      for (int step = 16; step > 0; step >>= 1)
-        if (kb + step < nb1 && rpre[kb + step] <= unit) kb += step;
+    int i = 0;
+    for (int kb = 0; kb < x.nblk; ++kb) {
+      if (!rsize[kb]) continue;
+      if (i++ % (kThreads / 32) != warp) continue;
+      const int64_t at = Ly.D + 16 * (static_cast<int64_t>(sh.X) + rpre[kb]);
+      if (!in_bounds(p.ctl, at, 16 * static_cast<int64_t>(rsize[kb]), p.stride)) continue;
+      uint16_t* dst = reinterpret_cast<uint16_t*>(payload + at);
       const uint8_t* buf = scr + kb * BB;
-      const uint32_t o = 2u * (P - 4u * rpre[kb]);  // first uint16 word within the record
-      if (!in_bounds(p.ctl, Ly.D + 16 * static_cast<int64_t>(sh.X) + 4 * static_cast<int64_t>(P),
-                     4, p.stride))
-        continue;
-      dst[P] = record_word(buf, static_cast<int>(LW), o) |
-               (record_word(buf, static_cast<int>(LW), o + 1) << 16);
+      const uint16_t* head = reinterpret_cast<const uint16_t*>(buf);
+      const uint32_t n = head[lane];
+      const uint32_t pre = head[kRansLanes + lane];
+      const uint16_t* src = reinterpret_cast<const uint16_t*>(buf + kRansBufHead) +
+                            (lane + 1) * LW - n;
+      dst[lane] = static_cast<uint16_t>(n);
+      uint16_t* d = dst + kRansLanes + pre;
+      for (uint32_t k = 0; k < n; ++k) d[k] = src[k];
+      const uint32_t words = kRansLanes + head[2 * kRansLanes];
+      if (words + lane < 8u * rsize[kb]) dst[words + lane] = 0;
     }
   }
   if (!direct_raw) {
@@ -579,18 +565,23 @@ __global__ void __launch_bounds__(kThreads)
 
 // A shard that went raw only at the end (its RANS payload would not have
 // been smaller than its raw bytes): rewrite it raw.  Shards that went raw
-// from the start were written raw by k_compress_rans itself.  A few CTAs per
-// SM walk all tiles (usually finding nothing to do).
+// from the start were written raw by k_compress_rans itself.  Every CTA
+// walks the ranks (one descriptor read each) and copies its share of the
+// tiles of those that need it, so a call with nothing to do costs R reads.
 __global__ void __launch_bounds__(kThreads) k_rans_raw_fixup(const CompressParams p) {
-  for (int64_t ti = blockIdx.x; ti < p.geo.total_tiles; ti += gridDim.x) {
-    const Tile x = decode_tile(p.geo, ti);
-    if (p.descs[x.rl].mode != CIERA_MODE_RAW) continue;
-    if (rans_layout(x.len, x.nb).D >= 2 * x.len) continue;
-    const uint4* w = reinterpret_cast<const uint4*>(p.w + x.shard_off + x.e0);
-    uint4* dst = reinterpret_cast<uint4*>(p.payloads + static_cast<int64_t>(x.rl) * p.stride +
-                                          2 * x.e0);
-    if (!in_bounds(p.ctl, 2 * x.e0, 2 * x.te, p.stride)) continue;
-    for (int64_t i = threadIdx.x; i < x.te / 8; i += blockDim.x) dst[i] = w[i];
+  const Geometry& g = p.geo;
+  for (int32_t rl = 0; rl < g.nfull + g.has_part; ++rl) {
+    if (p.descs[rl].mode != CIERA_MODE_RAW) continue;
+    const int64_t tiles = rl < g.nfull ? g.tiles_full : g.tiles_part;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+      const Tile x = make_tile(g, rl, t);
+      if (rans_layout(x.len, x.nb).D >= 2 * x.len) break;  // written raw directly
+      if (!in_bounds(p.ctl, 2 * x.e0, 2 * x.te, p.stride)) continue;
+      const uint4* w = reinterpret_cast<const uint4*>(p.w + x.shard_off + x.e0);
+      uint4* dst = reinterpret_cast<uint4*>(p.payloads + static_cast<int64_t>(x.rl) * p.stride +
+                                            2 * x.e0);
+      for (int64_t i = threadIdx.x; i < x.te / 8; i += blockDim.x) dst[i] = w[i];
+    }
   }
 }
 
@@ -839,7 +830,7 @@ int launch_compress_rans(const CompressParams& p, const uint32_t* hist_prev, uin
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const int64_t grid = p.geo.total_tiles < 4 * sms ? p.geo.total_tiles : 4 * sms;
+    const int64_t grid = p.geo.total_tiles < 2 * sms ? p.geo.total_tiles : 2 * sms;
     k_rans_raw_fixup<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
     e = cudaGetLastError();
   }
