@@ -116,3 +116,67 @@ def test_workload_4_layer_bucket_and_declines():
         bucket = torch.cat([full[o:o + k].view(torch.int16) for _, o, k in accepted]).view(
             torch.uint16)
         _check_iteration(ag, bucket, [0, 7], t, f"cfg4 layer0 t={t}")
+
+
+def _run_rans(wl, iterations, sampled):
+    """The RANS sender and receiver at full size: every iteration, sampled
+    ranks against the oracle byte for byte (payload, flags, descriptor,
+    histogram, caches, rebuilt values), the whole tensor by properties."""
+    dev = "cuda"
+    n = wl.layer_numel
+    R, B = wl.ranks, wl.block
+    ag = SimulatedAllgather(n, B, R, device=dev, keep_flags=True, rans=True)
+    ref = {}
+    for r in sampled:
+        ln = oracle.shard_len(n, R, r)
+        ref[r] = dict(sc=np.zeros(ln, np.uint8), rc=np.zeros(ln, np.uint8),
+                      hist=np.zeros(256, np.uint32))
+    w = workloads.initial_layer(wl, 0, dev)
+    modes = set()
+    for t in range(iterations):
+        if t > 0:
+            w = workloads.step_layer(wl, w, 0, t)
+        tag = f"{wl.name} rans t={t}"
+        shards = {r: to_np_u16(w[oracle.shard_begin(n, R, r):][:oracle.shard_len(n, R, r)])
+                  for r in sampled}
+        ag.step(w)
+        assert ag.status() == ciera.OK, tag
+        assert torch.equal(ag.out[:n].view(torch.int16), w.view(torch.int16)), tag
+        e = exps_dev(w)
+        assert torch.equal(ag.sender_cache[:n], e), tag
+        assert torch.equal(ag.recv_cache[:n], e), tag
+        descs = ag.descriptors()
+        hist_gpu = ag.hist[(t + 1) % 2].cpu().numpy().view(np.uint32)
+        for r in sampled:
+            b, ln = oracle.shard_begin(n, R, r), oracle.shard_len(n, R, r)
+            st = ref[r]
+            payload, flags, d, h = oracle.compress_shard_rans(shards[r], B, st["sc"], t == 0,
+                                                              st["hist"])
+            st["hist"] = h
+            gd = descs[r]
+            modes.add(int(d["mode"]))
+            assert (gd["mode"], gd["n_changed_blocks"], gd["body_bytes"], gd["payload_bytes"]) == (
+                d["mode"], d["n_changed_blocks"], d["body_bytes"], d["payload_bytes"]), (tag, r)
+            pb = int(d["payload_bytes"])
+            np.testing.assert_array_equal(to_np_u8(ag.payloads[r, :pb]), payload[:pb],
+                                          err_msg=f"{tag} rank {r} payload")
+            np.testing.assert_array_equal(to_np_u8(ag.flags[r, :len(flags)]), flags)
+            np.testing.assert_array_equal(hist_gpu[r], h, err_msg=f"{tag} rank {r} histogram")
+            np.testing.assert_array_equal(to_np_u8(ag.sender_cache[b:b + ln]), st["sc"])
+            rs, out = oracle.decompress_shard_any(payload, d, ln, B, st["rc"])
+            assert rs == 0
+            np.testing.assert_array_equal(to_np_u16(ag.out[b:b + ln]), out)
+            np.testing.assert_array_equal(to_np_u8(ag.recv_cache[b:b + ln]), st["rc"])
+    del ag
+    torch.cuda.empty_cache()
+    return modes
+
+
+def test_workload_2_rans_sender():
+    modes = _run_rans(workloads.workload(2), 3, sampled=[0, 15])
+    assert ciera.MODE_RANS in modes
+
+
+def test_workload_2_clustered_rans_sender():
+    modes = _run_rans(workloads.workload(2, "clustered0.1"), 3, sampled=[6])
+    assert ciera.MODE_RANS in modes
