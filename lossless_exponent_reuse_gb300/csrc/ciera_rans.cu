@@ -32,18 +32,19 @@
 //                      bytes to their fixed positions, the tile's exponents
 //                      into shared memory, the sampled histogram); one warp
 //                      per changed block codes it; decoupled look-back over
-//                      the record sizes places the records.
+//                      the record sizes places the records, which one warp
+//                      per block stores lane by lane.
 //   k_rans_raw_fixup   rewrites a shard raw when its RANS payload would not
 //                      have been smaller than the raw bytes.
 //   k_rans_dec_tables  one CTA per RANS rank: a slot -> (symbol, frequency,
 //                      bias) table of 4096 entries from the received
 //                      frequencies, so that a decoding step is one lookup.
-//   k_decompress_rans  one CTA per tile of a RAW rank (bulk copy of the
-//                      values, out and ExpCache) or of a RANS rank: bulk copies of the
-//                      sign+mantissa bytes and the records; the kept blocks
-//                      merge with their cached exponents; one warp per
-//                      changed block decodes it (slot table read through
-//                      L1) straight into the output and the ExpCache.
+//   k_decompress_rans  one CTA per tile.  RAW rank: a bulk copy of the
+//                      values, then out and ExpCache.  RANS rank: bulk copies
+//                      of the sign+mantissa bytes and the records; the kept
+//                      blocks merge with their cached exponents; one warp per
+//                      changed block decodes it (slot table read through L1)
+//                      straight into the output and the ExpCache.
 #include <cuda_runtime.h>
 
 #include <atomic>
