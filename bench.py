@@ -158,15 +158,20 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 def kernel_source_hash(kernel):
-    """sha256 prefix of the sources `kernel` is compiled from (its .cu file,
-    the shared device helpers and the launch parameters)."""
+    """sha256 prefix of the code `kernel` is compiled from (its .cu file, the
+    shared device helpers and the launch parameters), comments and white
+    space removed, so that only a change of code retires a profile."""
     import hashlib
+    import re
     csrc = os.path.join(ROOT, "lossless_exponent_reuse_gb300", "csrc")
     rans = kernel.endswith("_rans")
     units = ("ciera_rans.cu", "ciera_rans.h") if rans else ("ciera_kernels.cu",)
     h = hashlib.sha256()
     for name in units + ("ciera_device.cuh", "ciera_internal.h"):
-        h.update(open(os.path.join(csrc, name), "rb").read())
+        text = open(os.path.join(csrc, name)).read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
