@@ -174,7 +174,7 @@ __device__ uint32_t rans_encode_block(const uint8_t* exps, int L, const uint4* t
   int top = LW;
   uint32_t x = kRansLow;
   const int n = L > lane ? (L - lane + kRansLanes - 1) / kRansLanes : 0;  // this lane's symbols
-#pragma unroll 4
+#pragma unroll 8
   for (int m = n - 1; m >= 0; --m) {
     const uint4 E = tab[exps[lane + kRansLanes * m]];
     // x >= f * 2^20: emit the low 16 bits.  The store is unconditional (a
@@ -251,13 +251,13 @@ __device__ bool rans_decode_block(const uint16_t* rec, uint32_t rec_words, int L
   uint16_t* op = out + lane;
   uint8_t* rp = rc + lane;
   int m = 0;
-  for (; m + 4 <= n; m += 4) {
+  for (; m + 16 <= n; m += 16) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+    for (int k = 0; k < 16; ++k)
       decode_step(tab, s, last, sp + 32 * k, op + 32 * k, rp + 32 * k, x, idx, nxt);
-    sp += 128;
-    op += 128;
-    rp += 128;
+    sp += 512;
+    op += 512;
+    rp += 512;
   }
   for (; m < n; ++m) {
     decode_step(tab, s, last, sp, op, rp, x, idx, nxt);
