@@ -35,6 +35,8 @@ MODE_RANS = 2
 
 COLD = 1
 DECOMPRESS_RANS = 1
+SENDER_EXACT = 0
+SENDER_RANS = 1
 DEBUG_SKIP_FIRST_PUBLISH = 0x80000000
 DEBUG_OUT_OF_RANGE = 0x40000000  # accepted by checked builds only
 
@@ -60,7 +62,8 @@ class _Layer(ctypes.Structure):
                 ("payload_stride", ctypes.c_int64), ("descs_dev", ctypes.c_void_p),
                 ("recv_cache_dev", ctypes.c_void_p), ("out_dev", ctypes.c_void_p),
                 ("workspace_dev", ctypes.c_void_p), ("flags", ctypes.c_uint32),
-                ("pad", ctypes.c_uint32)]
+                ("sender", ctypes.c_uint32), ("hist_prev_dev", ctypes.c_void_p),
+                ("hist_out_dev", ctypes.c_void_p)]
 
 
 class _CostModel(ctypes.Structure):
@@ -393,12 +396,16 @@ class Pipeline:
             self._h = None
 
     def step(self, layers, inputs, stream=None) -> None:
-        """layers: SimulatedAllgather objects (exact sender); inputs: their
-        weights for this step.  Advances each layer's iteration count."""
+        """layers: SimulatedAllgather objects (exact or RANS sender); inputs:
+        their weights for this step.  Advances each layer's iteration count."""
         arr = (_Layer * len(layers))()
         for i, (ag, w) in enumerate(zip(layers, inputs)):
             if ag.hashed:
-                raise ValueError("the pipeline drives the exact sender")
+                raise ValueError("the pipeline drives the exact and the RANS senders")
+            hp = ho = None
+            if ag.rans:
+                hp = _dev_ptr(ag.hist[ag.iteration % 2], "hist_prev", torch.int32)
+                ho = _dev_ptr(ag.hist[(ag.iteration + 1) % 2], "hist_out", torch.int32)
             arr[i] = _Layer(ag.plan.handle.value, _dev_ptr(w, "w", torch.uint16),
                             _dev_ptr(ag.sender_cache, "sender_cache", torch.uint8),
                             _dev_ptr(ag.payloads, "payloads", torch.uint8),
@@ -406,7 +413,8 @@ class Pipeline:
                             _dev_ptr(ag.recv_cache, "recv_cache", torch.uint8),
                             _dev_ptr(ag.out, "out", torch.uint16),
                             _dev_ptr(ag.workspace, "workspace", torch.uint8),
-                            COLD if ag.iteration == 0 else 0, 0)
+                            COLD if ag.iteration == 0 else 0,
+                            SENDER_RANS if ag.rans else SENDER_EXACT, hp, ho)
         _check(lib().ciera_pipeline_step(self._h, arr, len(layers), _stream_handle(stream),
                                          self.side.cuda_stream), "ciera_pipeline_step")
         for ag in layers:

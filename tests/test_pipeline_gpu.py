@@ -77,3 +77,32 @@ def test_captured_pipelined_step_replays():
         for li, (a, b) in enumerate(zip(eager, graphed)):
             assert b.status() == ciera.OK
             _compare(a, b, f"replay t={t} layer {li}")
+
+
+RANS_LAYERS = [(131072, 4, 256), (196608, 3, 4096), (65536, 2, 272)]
+
+
+def test_pipelined_rans_step_equals_layer_by_layer():
+    """The same with the RANS sender (coded exponents) on every layer."""
+    seqs = []
+    for li, (n, R, B) in enumerate(RANS_LAYERS):
+        wl = workloads.small(f"R{li}", [(n,)], ranks=R, block=B, iterations=4, step=1e-3,
+                             seed=10 + li, p_block=0.2)
+        seqs.append([w.cuda() for w in workloads.sequence(wl, 4)])
+    seq_layers = [SimulatedAllgather(n, B, R, rans=True) for n, R, B in RANS_LAYERS]
+    pipe_layers = [SimulatedAllgather(n, B, R, rans=True) for n, R, B in RANS_LAYERS]
+    pipe = ciera.Pipeline(len(RANS_LAYERS))
+    modes = set()
+    for t in range(4):
+        for ag, s in zip(seq_layers, seqs):
+            ag.step(s[t])
+        pipe.step(pipe_layers, [s[t] for s in seqs])
+        torch.cuda.synchronize()
+        for li, (a, b) in enumerate(zip(seq_layers, pipe_layers)):
+            assert b.status() == ciera.OK
+            _compare(a, b, f"rans t={t} layer {li}")
+            assert all(torch.equal(x, y) for x, y in zip(a.hist, b.hist))
+            modes.update(d["mode"] for d in b.descriptors())
+            assert torch.equal(b.out[:RANS_LAYERS[li][0]].view(torch.int16),
+                               seqs[li][t].view(torch.int16))
+    assert ciera.MODE_RANS in modes
