@@ -189,6 +189,28 @@ def traffic_per_value(kernel):
     return None
 
 
+def instructions_per_value(kernel):
+    """Warp instructions per value of `kernel` from profiles/instructions.md
+    (ncu smsp__inst_executed.sum of one launch / values), or None if that
+    capture was taken on different kernel code."""
+    try:
+        h = kernel_source_hash(kernel)
+        for line in open(os.path.join(ROOT, "profiles", "instructions.md")):
+            cells = [c.strip() for c in line.strip().strip("|").split("|")]
+            if len(cells) >= 3 and cells[0] == kernel and cells[1] == h:
+                return float(cells[2])
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def issue_peak(device, sm_mhz):
+    """Warp instructions per second the GPU can issue: one per scheduler
+    (four per SM) per cycle, at the SM clock sampled during the run."""
+    props = torch.cuda.get_device_properties(device)
+    return props.multi_processor_count * 4 * sm_mhz * 1e6
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -516,6 +538,21 @@ def run_ours(args, world, rank, local):
         "gpu_launches": K * L * (6 if rans else 3),
         "clocks": clk,
     }
+
+    if rans and dom == "k_compress_rans":
+        # the RANS sender is bound by instruction issue, not by HBM: report it
+        # against the issue rate, with the HBM figures beside it
+        ipv = instructions_per_value("k_compress_rans")
+        mhz = (clk or {}).get("sm_mhz") or (clk or {}).get("sm_max_mhz") or 2070.0
+        ipk = issue_peak(dev, mhz) / 1e12
+        r = result["roofline"]
+        result["roofline"] = {
+            "bound": "alu", "kernel": dom,
+            "achieved": round(ipv * n / (dom_ms / 1e3) / 1e12, 4) if ipv else None,
+            "peak": round(ipk, 4), "unit": "T warp instructions/s",
+            "frac": round(ipv * n / (dom_ms / 1e3) / 1e12 / ipk, 4) if ipv else None,
+            "traffic": r["traffic"], "peak_kind": "issue rate at the sampled SM clock",
+            "hbm_achieved_gbs": r["achieved"], "hbm_frac": r["frac"]}
 
     del layers
     torch.cuda.empty_cache()
