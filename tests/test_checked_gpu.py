@@ -5,9 +5,8 @@ skipped and reported as CIERA_E_BOUNDS instead of touching memory.
 The GPU parity suites (small and full-size cases, graphs, the pipeline, the
 allocation-free entry point) run once more in a child process against the
 checked library (CIERA_CHECKED=1), which must give the same bytes and no
-status; the
-test hook CIERA_DEBUG_OUT_OF_RANGE, accepted only by the checked build,
-shows that the checks fire and that the library recovers."""
+status; the test hook CIERA_DEBUG_OUT_OF_RANGE, accepted only by the checked
+build, shows that the checks fire and that the library recovers."""
 import os
 import subprocess
 import sys
