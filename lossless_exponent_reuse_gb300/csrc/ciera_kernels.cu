@@ -337,51 +337,66 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
     if (kHashed) {
       // per-block sums of the two seeds' word terms
       if (stg) {
-        // Each thread sums its groups' terms in registers while they stay in
-        // one block and adds them to the block's sums when it moves on; at
-        // the end a warp whose lanes all sit in one block reduces first.
         const int ngroups = static_cast<int>(te >> 4);
         unsigned long long s1 = 0, s2 = 0;
-        int cur = -1;
-        for (int gi = ft; gi < ngroups; gi += kThreads - 32) {
-          const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
-          const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
-          const int64_t v0 = static_cast<int64_t>(gi) << 4;
-          const int kb = static_cast<int>(v0 / B);
-          const int64_t j0 = (v0 - kb * B) >> 3;  // first exponent word of the group
-          const unsigned long long lo =
-              exp4(w0.x, w0.y) | (static_cast<unsigned long long>(exp4(w0.z, w0.w)) << 32);
-          const unsigned long long hi =
-              exp4(w1.x, w1.y) | (static_cast<unsigned long long>(exp4(w1.z, w1.w)) << 32);
-          unsigned long long a1, a2, b1, b2;
-          hash_word(lo, j0, a1, a2);
-          hash_word(hi, j0 + 1, b1, b2);
-          if (kb != cur) {
-            if (cur >= 0) {
-              atomicAdd(&bsum[2 * cur], s1);
-              atomicAdd(&bsum[2 * cur + 1], s2);
-            }
-            s1 = s2 = 0;
-            cur = kb;
-          }
-          s1 += a1 + b1;
-          s2 += a2 + b2;
-        }
-        const int cur0 = __shfl_sync(0xffffffffu, cur, 0);
-        if (__all_sync(0xffffffffu, cur == cur0)) {
+        // The loop runs whole warps over 32 consecutive groups at a time.  A
+        // warp whose groups all lie in one block keeps running sums in
+        // registers; when its block changes it reduces them across the warp
+        // and lane 0 adds them to the block's sums.  A warp straddling two
+        // blocks (blocks of fewer than 512 values) adds lane by lane.
+        const int G = static_cast<int>(B / 16);  // groups per block
+        int cur = -1;                            // block of the running sums (warp-uniform)
+        auto flush = [&]() {
+          if (cur < 0) return;
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) {
             s1 += __shfl_xor_sync(0xffffffffu, s1, o);
             s2 += __shfl_xor_sync(0xffffffffu, s2, o);
           }
-          if (lane == 0 && cur >= 0) {
+          if (lane == 0) {
             atomicAdd(&bsum[2 * cur], s1);
             atomicAdd(&bsum[2 * cur + 1], s2);
           }
-        } else if (cur >= 0) {
-          atomicAdd(&bsum[2 * cur], s1);
-          atomicAdd(&bsum[2 * cur + 1], s2);
+          s1 = s2 = 0;
+          cur = -1;
+        };
+        for (int g0 = ft - lane; g0 < ngroups; g0 += kThreads - 32) {
+          const int gi = g0 + lane;
+          const bool in = gi < ngroups;
+          int kb = -1;
+          unsigned long long t1 = 0, t2 = 0;
+          if (in) {
+            const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
+            const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
+            kb = gi / G;
+            const int64_t j0 = 2 * static_cast<int64_t>(gi - kb * G);  // first exponent word
+            const unsigned long long lo =
+                exp4(w0.x, w0.y) | (static_cast<unsigned long long>(exp4(w0.z, w0.w)) << 32);
+            const unsigned long long hi =
+                exp4(w1.x, w1.y) | (static_cast<unsigned long long>(exp4(w1.z, w1.w)) << 32);
+            unsigned long long a1, a2, b1, b2;
+            hash_word(lo, j0, a1, a2);
+            hash_word(hi, j0 + 1, b1, b2);
+            t1 = a1 + b1;
+            t2 = a2 + b2;
+          }
+          const int kb0 = __shfl_sync(0xffffffffu, kb, 0);  // lane 0 is always in
+          const bool uniform = __all_sync(0xffffffffu, !in || kb == kb0);
+          if (!(uniform && kb0 == cur)) {
+            flush();
+            if (!uniform) {
+              if (in) {
+                atomicAdd(&bsum[2 * kb], t1);
+                atomicAdd(&bsum[2 * kb + 1], t2);
+              }
+              continue;
+            }
+            cur = kb0;
+          }
+          s1 += t1;
+          s2 += t2;
         }
+        flush();
       } else {
         const int64_t wpb = (B + 7) / 8;  // exponent words per block
         const int64_t nwords = static_cast<int64_t>(x.nblk) * wpb;
