@@ -257,3 +257,35 @@ def test_rans_receiver_rejects_compressed_payloads():
     assert any(d["mode"] == ciera.MODE_COMPRESSED for d in ag.descriptors())
     ag.plan.decompress(ag.payloads, ag.descs, ag.recv_cache, ag.out, ag.workspace, rans=True)
     assert ag.status() == ciera.E_CORRUPT
+
+
+def test_rans_rank_ranges_match_full_launch():
+    """One RANS call per rank (each with its own histogram rows and the
+    payload, descriptor and flag rows of that rank) gives the bytes of one
+    call over all ranks, including the partial shard."""
+    n, R, B = 131056, 32, 1024
+    seq = rans_sequence(n, B, seed=21)[:4]
+    full = SimulatedAllgather(n, B, R, keep_flags=True, rans=True)
+    part = SimulatedAllgather(n, B, R, keep_flags=True, rans=True)
+    S = full.plan.info.shard_len
+    for t, w in enumerate(seq):
+        wd = torch.from_numpy(w.view(np.int16)).cuda().view(torch.uint16)
+        full.compress(wd)
+        prev, cur = part.hist[t % 2], part.hist[(t + 1) % 2]
+        for r in range(R):
+            lo, hi = r * S, min(n, (r + 1) * S)
+            part.plan.compress_rans(wd[lo:hi], part.sender_cache[lo:hi], prev[r:r + 1],
+                                    cur[r:r + 1], part.payloads[r:r + 1], part.descs[r:r + 1],
+                                    part.workspace, cold=t == 0, rank_begin=r, rank_count=1,
+                                    flags_out=part.flags[r:r + 1])
+        assert part.status() == ciera.OK
+        assert full.descriptors() == part.descriptors(), t
+        for r, d in enumerate(full.descriptors()):
+            pb = d["payload_bytes"]
+            assert torch.equal(full.payloads[r, :pb], part.payloads[r, :pb]), (t, r)
+        assert torch.equal(full.flags, part.flags)
+        assert torch.equal(full.sender_cache, part.sender_cache)
+        assert torch.equal(full.hist[(t + 1) % 2], cur)
+        full.decompress()
+        part.iteration += 1
+        assert torch.equal(full.out[:n].view(torch.int16), wd.view(torch.int16))
