@@ -60,6 +60,9 @@ def parse_args():
     ap.add_argument("--sender", choices=["exact", "hash", "rans"], default="exact",
                     help="change test: exact exponent compare (default) or the 128-bit "
                          "block hash with a 16-byte-per-block HashCache")
+    ap.add_argument("--no-raw-ahead", action="store_true",
+                    help="exact/hash senders: every shard takes the look-back scan, "
+                         "even those predicted raw")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -343,7 +346,9 @@ def run_ours(args, world, rank, local):
     gen = iteration_buckets(wl, W + K, dev)
     hashed = args.sender == "hash"
     rans = args.sender == "rans"
-    layers = [SimulatedAllgather(n, wl.block, wl.ranks, device=dev, hashed=hashed, rans=rans)
+    raw_ahead = not args.no_raw_ahead
+    layers = [SimulatedAllgather(n, wl.block, wl.ranks, device=dev, hashed=hashed, rans=rans,
+                                 raw_ahead=raw_ahead)
               for _ in range(L)]
     stream = torch.cuda.current_stream()
     warm_host = []                                  # iterations W-1, W of layer 0 for the oracle
@@ -515,6 +520,10 @@ def run_ours(args, world, rank, local):
            "l2": f"inputs larger than L2 ({2 * n / 1e6:.0f} MB of weights per plan), no flush"}
     if declined:
         cfg["declined_values_per_layer"] = declined
+    info0 = layers[0].plan.info
+    repack = int(raw_ahead and not rans and bool(info0.fast_path) and info0.tile_blocks <= 32)
+    if not rans:
+        cfg["raw_ahead"] = bool(repack)
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(total_s * 1e3 / K, 4),
@@ -533,9 +542,10 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "peak_kind": peak_kind},
-        # exact/hashed: compress, bitmap scan, decompress; RANS: coder tables,
-        # compress, raw fixup, bitmap scan, slot tables, decompress
-        "gpu_launches": K * L * (6 if rans else 3),
+        # exact/hashed: compress, repack (raw-ahead plans), bitmap scan,
+        # decompress; RANS: coder tables, compress, raw fixup, bitmap scan,
+        # slot tables, decompress
+        "gpu_launches": K * L * (6 if rans else 3 + repack),
         "clocks": clk,
     }
 
@@ -558,7 +568,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.empty_cache()
     if not args.no_e2e:
         if L == 1:
-            result["e2e"] = run_e2e(wl, [s_[0] for s_ in seq], n, K, dev, world, hashed, rans)
+            result["e2e"] = run_e2e(wl, [s_[0] for s_ in seq], n, K, dev, world, hashed, rans,
+                                    raw_ahead)
         else:
             result["e2e"] = None
     del seq
@@ -567,7 +578,7 @@ def run_ours(args, world, rank, local):
     return result
 
 
-def run_e2e(wl, seq, n, K, dev, world, hashed=False, rans=False):
+def run_e2e(wl, seq, n, K, dev, world, hashed=False, rans=False, raw_ahead=True):
     """The same metric through host buffers: each step copies its weights
     from pinned host memory, runs the path and copies the rebuilt weights
     back, with neighbouring steps' uploads and downloads overlapped
@@ -577,7 +588,8 @@ def run_e2e(wl, seq, n, K, dev, world, hashed=False, rans=False):
     from lossless_exponent_reuse_gb300.allgather import HostStreamer, SimulatedAllgather
     host = [s.view(torch.int16).to("cpu").pin_memory() for s in seq]
     outs = [torch.empty(n, dtype=torch.int16).pin_memory() for _ in range(2)]
-    ag = SimulatedAllgather(n, wl.block, wl.ranks, device=dev, hashed=hashed, rans=rans)
+    ag = SimulatedAllgather(n, wl.block, wl.ranks, device=dev, hashed=hashed, rans=rans,
+                            raw_ahead=raw_ahead)
     hs = HostStreamer(ag)
     stream = torch.cuda.current_stream()
     for t in range(min(3, len(host))):               # warm-up (first call is the cold start)

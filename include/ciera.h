@@ -75,10 +75,12 @@ extern "C" {
 
 /* ciera_compress flags */
 #define CIERA_COLD 1u            /* no previous exponents: every block changed, payload raw */
+#define CIERA_NO_RAW_AHEAD 2u    /* every shard takes the look-back scan (no raw-ahead) */
 /* ciera_decompress flags */
 #define CIERA_DECOMPRESS_RANS 1u /* payloads of ciera_compress_rans: RAW or RANS */
 /* Test hook: the first tile of every shard never publishes its prefix, so
- * that the tiles after it run into the bounded wait (CIERA_E_TIMEOUT). */
+ * that the tiles after it (for a raw-ahead shard: its last tile) run into
+ * the bounded wait (CIERA_E_TIMEOUT). */
 #define CIERA_DEBUG_SKIP_FIRST_PUBLISH 0x80000000u
 /* Test hook of checked builds only (a library built with -DCIERA_CHECKED;
  * other builds reject the flag with CIERA_E_INVAL): ciera_compress moves
@@ -150,10 +152,24 @@ int ciera_workspace_init(ciera_plan_t plan, void *workspace_dev, void *stream);
  *   flags_dev        optional (may be NULL): rank_count rows of
  *                    blocks_per_shard bytes, 1 = block changed
  *   workspace_dev    info.workspace_bytes bytes, see the conventions above
- *   flags            CIERA_COLD, or 0
+ *   flags            CIERA_COLD and/or CIERA_NO_RAW_AHEAD, or 0
  * Errors: CIERA_E_INVAL for a bad range, NULL pointer or short stride;
  * CIERA_E_CUDA if a launch fails.  CIERA_E_TIMEOUT appears later through
- * ciera_status(). */
+ * ciera_status().
+ *
+ * Raw-ahead.  The offsets of a compressed body depend on the changed blocks
+ * of every earlier tile of the shard (the prefix scan that Algorithm 1
+ * walks as "j <- j+1"), found by a look-back between the tiles' CTAs.  A
+ * RAW payload needs no offsets.  A shard whose previous payload from this
+ * workspace was RAW (for instance, every block of 4096 values changes each
+ * step), and every shard of a cold call, is predicted RAW: its tiles store
+ * their values at their raw positions without the look-back, and the
+ * shard's last tile sums the tiles' changed blocks.  If the shard is not
+ * RAW after all, a second kernel on the same stream rewrites its payload
+ * compacted.  The bytes produced are the same either way; a wrong guess
+ * costs one more read of the shard.  It applies where the staged path runs
+ * (fast_path) with blocks of at least 256 values on shards of a multiple of
+ * 16 values; CIERA_NO_RAW_AHEAD turns it off for a call. */
 int ciera_compress(ciera_plan_t plan, int rank_begin, int rank_count, const uint16_t *w_dev,
                    uint8_t *sender_cache_dev, uint8_t *payloads_dev, int64_t payload_stride,
                    ciera_desc *descs_dev, uint8_t *flags_dev, void *workspace_dev, uint32_t flags,

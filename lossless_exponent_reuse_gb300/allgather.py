@@ -22,7 +22,8 @@ class SimulatedAllgather:
     """Device state of one plan: both exponent caches, payloads, descriptors."""
 
     def __init__(self, numel: int, block: int, ranks: int, device="cuda",
-                 keep_flags: bool = False, hashed: bool = False, rans: bool = False):
+                 keep_flags: bool = False, hashed: bool = False, rans: bool = False,
+                 raw_ahead: bool = True):
         if hashed and rans:
             raise ValueError("the hashed change test and RANS payloads are separate senders")
         self.plan = ciera.Plan(numel, block, ranks)
@@ -31,6 +32,8 @@ class SimulatedAllgather:
         self.device = torch.device(device)
         self.hashed = hashed
         self.rans = rans
+        # raw_ahead=False: every shard takes the look-back scan (same bytes)
+        self.extra_flags = 0 if raw_ahead else ciera.NO_RAW_AHEAD
         # RANS: each shard's exponent histogram, this call's and the previous one's
         self.hist = ([torch.zeros((ranks, 256), dtype=torch.int32, device=device)
                       for _ in range(2)] if rans else None)
@@ -57,10 +60,12 @@ class SimulatedAllgather:
         elif self.hashed:
             self.plan.compress_hashed(w, self.hash_cache, self.payloads, self.descs,
                                       self.workspace, cold=self.iteration == 0,
-                                      flags_out=self.flags, stream=stream)
+                                      flags_out=self.flags, extra_flags=self.extra_flags,
+                                      stream=stream)
         else:
             self.plan.compress(w, self.sender_cache, self.payloads, self.descs, self.workspace,
-                               cold=self.iteration == 0, flags_out=self.flags, stream=stream)
+                               cold=self.iteration == 0, flags_out=self.flags,
+                               extra_flags=self.extra_flags, stream=stream)
 
     def decompress(self, stream=None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
         o = self.out if out is None else out

@@ -34,6 +34,7 @@ MODE_RAW = 1
 MODE_RANS = 2
 
 COLD = 1
+NO_RAW_AHEAD = 2  # compress: every shard takes the look-back scan
 DECOMPRESS_RANS = 1
 SENDER_EXACT = 0
 SENDER_RANS = 1
@@ -248,7 +249,8 @@ class Plan:
     def compress_hashed(self, w: torch.Tensor, hash_cache: torch.Tensor, payloads: torch.Tensor,
                         descs: torch.Tensor, workspace: torch.Tensor, *, cold: bool = False,
                         rank_begin: int = 0, rank_count: Optional[int] = None,
-                        flags_out: Optional[torch.Tensor] = None, stream=None) -> None:
+                        flags_out: Optional[torch.Tensor] = None, extra_flags: int = 0,
+                        stream=None) -> None:
         """ciera_compress_hashed: ``hash_cache`` holds 16 bytes per block
         (rank_count x blocks_per_shard x 2 uint64, any 8-byte dtype)."""
         info = self.info
@@ -266,7 +268,7 @@ class Plan:
             _dev_ptr(hash_cache, "hash_cache"),
             _dev_ptr(payloads, "payloads", torch.uint8), payloads.stride(0),
             _dev_ptr(descs, "descs", torch.uint8), _dev_ptr(flags_out, "flags_out", torch.uint8),
-            _dev_ptr(workspace, "workspace", torch.uint8), COLD if cold else 0,
+            _dev_ptr(workspace, "workspace", torch.uint8), (COLD if cold else 0) | int(extra_flags),
             _stream_handle(stream)), "ciera_compress_hashed")
 
     def compress_rans(self, w: torch.Tensor, sender_cache: torch.Tensor,
@@ -413,7 +415,7 @@ class Pipeline:
                             _dev_ptr(ag.recv_cache, "recv_cache", torch.uint8),
                             _dev_ptr(ag.out, "out", torch.uint16),
                             _dev_ptr(ag.workspace, "workspace", torch.uint8),
-                            COLD if ag.iteration == 0 else 0,
+                            (COLD if ag.iteration == 0 else 0) | ag.extra_flags,
                             SENDER_RANS if ag.rans else SENDER_EXACT, hp, ho)
         _check(lib().ciera_pipeline_step(self._h, arr, len(layers), _stream_handle(stream),
                                          self.side.cuda_stream), "ciera_pipeline_step")

@@ -23,10 +23,10 @@ using namespace ciera;
 // Flags every compress entry point accepts; the out-of-range test hook only
 // in checked builds, where the kernels skip the accesses it provokes.
 #ifdef CIERA_CHECKED
-constexpr uint32_t kCompressFlags =
-    CIERA_COLD | CIERA_DEBUG_SKIP_FIRST_PUBLISH | CIERA_DEBUG_OUT_OF_RANGE;
+constexpr uint32_t kCompressFlags = CIERA_COLD | CIERA_NO_RAW_AHEAD |
+                                    CIERA_DEBUG_SKIP_FIRST_PUBLISH | CIERA_DEBUG_OUT_OF_RANGE;
 #else
-constexpr uint32_t kCompressFlags = CIERA_COLD | CIERA_DEBUG_SKIP_FIRST_PUBLISH;
+constexpr uint32_t kCompressFlags = CIERA_COLD | CIERA_NO_RAW_AHEAD | CIERA_DEBUG_SKIP_FIRST_PUBLISH;
 #endif
 
 struct ciera_plan_s {
@@ -46,6 +46,7 @@ struct ciera_plan_s {
   int64_t nw_stride;
   int64_t off_status, off_tflags, off_flags, off_words, off_prefix, off_rstate;
   int64_t off_renc, off_rdec;  // per-rank RANS coder tables (encoder, decoder)
+  int64_t off_pred, off_result;  // per-rank raw-ahead prediction and launch result
   int64_t ws_bytes;
   int64_t smem_flags;         // flag words of every compress call (exact test)
   int64_t smem_flags_hashed;  // ... plus the per-block hash sums (hashed test)
@@ -149,7 +150,9 @@ int ciera_plan(const int64_t* shape, int ndim, int64_t block, int ranks, ciera_p
   p->off_rstate = align_up(p->off_prefix + 4 * p->nw_stride * ranks, 256);
   p->off_renc = align_up(p->off_rstate + 4 * static_cast<int64_t>(ranks), 256);
   p->off_rdec = align_up(p->off_renc + kRansEncTableBytes * ranks, 256);
-  p->ws_bytes = align_up(p->off_rdec + kRansDecTableBytes * ranks, 256);
+  p->off_pred = align_up(p->off_rdec + kRansDecTableBytes * ranks, 256);
+  p->off_result = align_up(p->off_pred + 4 * static_cast<int64_t>(ranks), 256);
+  p->ws_bytes = align_up(p->off_result + 8 * static_cast<int64_t>(ranks), 256);
   p->fast = (block % 16 == 0) && block >= kFastMinBlock && block <= kFastMaxBlock &&
             (p->S % 16 == 0);
   // compress: flag words + their prefix (every call), then 2*TE values and
@@ -230,9 +233,14 @@ int compress_impl(ciera_plan_t p, int rank_begin, int rank_count, const uint16_t
   kp.fast = p->fast && aligned16(w_dev) && aligned16(payloads_dev) &&
             (payload_stride % 16 == 0) &&
             (hashed ? aligned16(hash_cache_dev) : aligned16(sender_cache_dev));
+  // raw-ahead needs staged tiles of at most 32 blocks (flag bits in one word)
+  kp.raw_ahead = kp.fast && p->T <= 32 && !(flags & CIERA_NO_RAW_AHEAD) ? 1 : 0;
+  kp.pred = reinterpret_cast<uint32_t*>(ws + p->off_pred) + rank_begin;
+  kp.result = reinterpret_cast<unsigned long long*>(ws + p->off_result) + rank_begin;
   const int64_t flag_region = hashed ? p->smem_flags_hashed : p->smem_flags;
   const int64_t smem = flag_region + (kp.fast ? 3 * p->T * p->block : 0);
-  const int e = launch_compress(kp, smem, p->raw_fixup ? 1 : 0, stream);
+  const int64_t repack_smem = 128 + 3 * p->T * p->block + 4 * ceil_div(rank_count, 32);
+  const int e = launch_compress(kp, smem, p->raw_fixup ? 1 : 0, repack_smem, stream);
   return e == cudaSuccess ? CIERA_OK : CIERA_E_CUDA;
 }
 

@@ -43,6 +43,13 @@ enum : uint32_t {
 //   changed blocks (aggregate of the tile, or inclusive prefix in its shard).
 enum : uint32_t { kStateAggregate = 1u, kStateInclusive = 2u };
 
+// Per-shard outcome of a compress launch (result word: launch tag << 32 |
+// these bits), read by k_repack after the launch.
+enum : uint32_t {
+  kResultRepack = 1u,  // raw-ahead shard that is not raw: rewrite it compacted
+  kResultRaw = 2u,     // the shard's payload is RAW (the next call predicts raw)
+};
+
 // Receiver per-rank state written by the bitmap scan.
 enum : uint32_t { kRankSkip = 0u, kRankCompressed = 1u, kRankRaw = 2u, kRankRans = 3u };
 
@@ -98,9 +105,12 @@ struct CompressParams {
   Control* ctl;
   uint64_t timeout_ns;
   uint32_t flags;
-  uint32_t pad2;
+  int32_t raw_ahead;            // 1: shards predicted raw skip the look-back
   int32_t fast;                 // staged path allowed for whole-16 tiles
   int32_t hashed;               // 1: hashed change test (k_compress<true>)
+  uint32_t* pred;               // per range rank: 1 if its last payload was RAW
+                                // (read by k_compress, rewritten by k_repack)
+  unsigned long long* result;   // per range rank: launch tag << 32 | kResult* bits
 };
 
 struct DecompressParams {
@@ -122,7 +132,10 @@ struct DecompressParams {
 
 // Launchers (ciera_kernels.cu).  Return a cudaError_t value.
 // smem_bytes: dynamic shared memory of one CTA.
-int launch_compress(const CompressParams& p, int64_t smem_bytes, int raw_fixup, void* stream);
+// With p.raw_ahead, also launches k_repack (repack_smem bytes of dynamic
+// shared memory per CTA).
+int launch_compress(const CompressParams& p, int64_t smem_bytes, int raw_fixup,
+                    int64_t repack_smem, void* stream);
 int launch_decompress(const DecompressParams& p, int64_t smem_bytes, void* stream);
 
 }  // namespace ciera

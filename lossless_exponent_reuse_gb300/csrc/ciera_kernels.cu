@@ -13,6 +13,9 @@
 //                    over the bitmap, as a single-pass scan), pack, sender
 //                    cache refresh, and -- in the shard's last tile -- the
 //                    descriptor and the bitmap.
+//   k_repack         after k_compress when raw-ahead is on: rewrites, in
+//                    compacted layout, the shards predicted raw that were not,
+//                    and records every shard's mode as the next prediction.
 //   k_raw_fixup      only for plans where a raw payload can still contain
 //                    unchanged blocks (tiny B): rewrites such payloads raw.
 //   k_bitmap_scan    receiver: validates each descriptor against its bitmap
@@ -114,6 +117,8 @@ struct CompressShared {
   uint32_t X;     // changed blocks before the tile in its shard
   uint32_t agg;   // changed blocks in the tile
   uint32_t bad;   // a bounded wait ran out on this tile
+  uint32_t ahead; // raw-ahead tile: values stored at their raw positions, no look-back
+  uint32_t red[kThreads / 32];  // per-warp sums of the raw-ahead finish
 };
 
 // Warps 1-3, after the flag bits are final: flag bytes, popcount prefix,
@@ -143,37 +148,33 @@ __device__ void publish_aggregate(const CompressParams& p, const Tile& x, const 
     }
     sh.agg = run;
     const bool skip = (p.flags & CIERA_DEBUG_SKIP_FIRST_PUBLISH) && x.t == 0;
-    if (!skip) publish(p, x, sh.epoch, x.t == 0 ? kStateInclusive : kStateAggregate, run);
+    // a raw-ahead shard's tiles publish aggregates only; its last tile turns
+    // them into prefixes where a rewrite needs them
+    const uint32_t state = x.t == 0 && !sh.ahead ? kStateInclusive : kStateAggregate;
+    if (!skip) publish(p, x, sh.epoch, state, run);
   }
   (void)s0;
 }
 
-// Last tile of a shard: descriptor and bitmap.
-__device__ void compress_epilogue(const CompressParams& p, const Tile& x, const CompressShared& sh,
-                                  const uint32_t* fw) {
-  const int tid = threadIdx.x;
-  const int64_t B = p.geo.B;
-  const uint32_t total = sh.X + sh.agg;  // changed blocks in the shard
+// Body size of a shard (len values, nb blocks) with `total` changed blocks;
+// last_changed: its last (possibly partial) block changed.
+__device__ __forceinline__ int64_t body_bytes_of(const Tile& x, int64_t B, uint32_t total,
+                                                 bool last_changed) {
   const int64_t last_len = x.len - (x.nb - 1) * B;
-  const bool last_changed = flag_of(fw, static_cast<int>(x.nb - 1 - x.k0));
   const int64_t changed_vals =
       static_cast<int64_t>(total) * B - (last_changed ? (B - last_len) : 0);
-  const int64_t body = x.len + changed_vals;
-  const int64_t bm = (x.nb + 7) / 8;
-  const bool raw = (p.flags & CIERA_COLD) || (body + bm >= 2 * x.len);
+  return x.len + changed_vals;
+}
+
+// The shard's bitmap (bm bytes) at payload offset `body`, all threads of the
+// CTA.  Every tile of the shard wrote its flags during this launch.
+__device__ void write_bitmap(const CompressParams& p, const Tile& x, uint32_t epoch,
+                             int64_t body, int64_t bm) {
+  const int tid = threadIdx.x;
   uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
-  if (tid == 0) {
-    ciera_desc d;
-    d.mode = raw ? CIERA_MODE_RAW : CIERA_MODE_COMPRESSED;
-    d.n_changed_blocks = total;
-    d.body_bytes = static_cast<uint64_t>(raw ? 2 * x.len : body);
-    d.payload_bytes = static_cast<uint64_t>(raw ? 2 * x.len : body + bm);
-    p.descs[x.rl] = d;
-  }
-  if (raw) return;
   if (flags_in_words(p)) {
-    // every tile of the shard stored its flag bits with this call's epoch;
-    // wait (bounded) until each word shows it
+    // each tile stored its flag bits with this launch's tag; wait (bounded)
+    // until each word shows it
     const unsigned long long* tf = p.tile_flags + (x.sidx - x.t);
     const int64_t T = p.geo.T;
     bool to = false;
@@ -188,9 +189,9 @@ __device__ void compress_epilogue(const CompressParams& p, const Tile& x, const 
         if (tj != cur) {
           cur = tj;
           unsigned long long v = ld_relaxed_u64(tf + tj);
-          if ((v >> 32) != sh.epoch) {
+          if ((v >> 32) != epoch) {
             const uint64_t t0 = globaltimer();
-            while ((v >> 32) != sh.epoch) {
+            while ((v >> 32) != epoch) {
               if (globaltimer() - t0 > p.timeout_ns) {
                 to = true;
                 break;
@@ -219,6 +220,130 @@ __device__ void compress_epilogue(const CompressParams& p, const Tile& x, const 
       if (in_bounds(p.ctl, body + i, 1, p.stride)) payload[body + i] = static_cast<uint8_t>(byte);
     }
   }
+}
+
+// Last tile of a shard: descriptor and bitmap.
+__device__ void compress_epilogue(const CompressParams& p, const Tile& x, const CompressShared& sh,
+                                  const uint32_t* fw) {
+  const int tid = threadIdx.x;
+  const uint32_t total = sh.X + sh.agg;  // changed blocks in the shard
+  const bool last_changed = flag_of(fw, static_cast<int>(x.nb - 1 - x.k0));
+  const int64_t body = body_bytes_of(x, p.geo.B, total, last_changed);
+  const int64_t bm = (x.nb + 7) / 8;
+  const bool raw = (p.flags & CIERA_COLD) || (body + bm >= 2 * x.len);
+  if (tid == 0) {
+    ciera_desc d;
+    d.mode = raw ? CIERA_MODE_RAW : CIERA_MODE_COMPRESSED;
+    d.n_changed_blocks = total;
+    d.body_bytes = static_cast<uint64_t>(raw ? 2 * x.len : body);
+    d.payload_bytes = static_cast<uint64_t>(raw ? 2 * x.len : body + bm);
+    p.descs[x.rl] = d;
+    if (p.raw_ahead)
+      p.result[x.rl] = (static_cast<unsigned long long>(sh.epoch) << 32) | (raw ? kResultRaw : 0u);
+  }
+  if (raw) return;
+  write_bitmap(p, x, sh.epoch, body, bm);
+}
+
+// Last tile of a raw-ahead shard, all threads.  Every tile of the shard
+// stored its values at their raw positions and published only its
+// aggregate.  Sum the aggregates (each thread a contiguous run of tiles,
+// waiting, bounded, for tiles still running) and write the descriptor.  A
+// raw shard is then complete.  Otherwise every tile's status word is
+// rewritten as its inclusive prefix and the shard is left to k_repack, which
+// rewrites the payload compacted and appends the bitmap (the raw stores of
+// other tiles may still be in flight, so nothing is compacted here).
+__device__ void raw_ahead_finish(const CompressParams& p, const Tile& x, CompressShared& sh,
+                                 const uint32_t* fw) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t n = x.tiles;
+  const int64_t chunk = (n + kThreads - 1) / kThreads;
+  const int64_t i0 = tid * chunk < n ? tid * chunk : n;
+  const int64_t i1 = i0 + chunk < n ? i0 + chunk : n;
+  unsigned long long* st = p.tile_status + (x.sidx - x.t);
+  const uint32_t epoch = sh.epoch;
+  bool to = false;
+  uint32_t sum = 0;
+  for (int64_t i = i0; i < i1 && !to; ++i) {
+    unsigned long long v = ld_relaxed_u64(st + i);
+    if ((v >> 32) != epoch || ((v >> 30) & 3ull) == 0) {
+      const uint64_t t0 = globaltimer();
+      while ((v >> 32) != epoch || ((v >> 30) & 3ull) == 0) {
+        if (globaltimer() - t0 > p.timeout_ns) {
+          to = true;
+          break;
+        }
+        __nanosleep(256);
+        v = ld_relaxed_u64(st + i);
+      }
+    }
+    sum += static_cast<uint32_t>(v & 0x3FFFFFFFull);
+  }
+  // exclusive prefix of the per-thread sums across the CTA
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) sh.red[warp] = incl;
+  const bool any_to = __syncthreads_or(to);
+  uint32_t base = 0, total = 0;
+#pragma unroll
+  for (int w2 = 0; w2 < kThreads / 32; ++w2) {
+    base += w2 < warp ? sh.red[w2] : 0u;
+    total += sh.red[w2];
+  }
+  if (total > x.nb) total = static_cast<uint32_t>(x.nb);  // only after a timeout
+  const bool last_changed = flag_of(fw, static_cast<int>(x.nb - 1 - x.k0));
+  const int64_t body = body_bytes_of(x, p.geo.B, total, last_changed);
+  const int64_t bm = (x.nb + 7) / 8;
+  const bool raw = (p.flags & CIERA_COLD) || (body + bm >= 2 * x.len);
+  if (!raw && !any_to) {
+    const unsigned long long tag = (static_cast<unsigned long long>(epoch) << 32) |
+                                   (static_cast<unsigned long long>(kStateInclusive) << 30);
+    uint32_t run = base + incl - sum;
+    for (int64_t i = i0; i < i1; ++i) {
+      run += static_cast<uint32_t>(ld_relaxed_u64(st + i) & 0x3FFFFFFFull);
+      st_relaxed_u64(st + i, tag | run);
+    }
+  }
+  if (tid == 0) {
+    if (any_to) record_status(p.ctl, kStatusTimeout);
+    ciera_desc d;
+    d.mode = raw ? CIERA_MODE_RAW : CIERA_MODE_COMPRESSED;
+    d.n_changed_blocks = total;
+    d.body_bytes = static_cast<uint64_t>(raw ? 2 * x.len : body);
+    d.payload_bytes = static_cast<uint64_t>(raw ? 2 * x.len : body + bm);
+    p.descs[x.rl] = d;
+    const uint32_t res = any_to ? 0u : raw ? kResultRaw : kResultRepack;
+    p.result[x.rl] = (static_cast<unsigned long long>(epoch) << 32) | res;
+  }
+}
+
+// Thread 0 of a staged tile: bulk stores of the body, one per maximal run of
+// equally flagged blocks -- changed runs from the values (ws), unchanged runs
+// from their sign+mantissa bytes (cs) -- at offsets that follow from X, the
+// changed blocks before the tile in its shard.
+__device__ void store_runs(const CompressParams& p, const Tile& x, const uint32_t* fw,
+                           const uint32_t* fpre, uint32_t X, const uint8_t* ws, const uint8_t* cs) {
+  const int64_t B = p.geo.B;
+  uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
+  int ka = 0;
+  while (ka < x.nblk) {
+    const bool f = flag_of(fw, ka);
+    int kz = ka + 1;
+    while (kz < x.nblk && flag_of(fw, kz) == f) ++kz;
+    const int64_t ea = static_cast<int64_t>(ka) * B;
+    const int64_t ez = static_cast<int64_t>(kz) * B < x.te ? static_cast<int64_t>(kz) * B : x.te;
+    int64_t off = (x.k0 + ka + X + count_before(fw, fpre, ka)) * B;
+    if (kChecked && (p.flags & CIERA_DEBUG_OUT_OF_RANGE)) off += int64_t(1) << 40;
+    const int64_t bytes = (f ? 2 : 1) * (ez - ea);
+    if (in_bounds(p.ctl, off, bytes, p.stride))
+      bulk_s2g(payload + off, f ? ws + 2 * ea : cs + ea, static_cast<uint32_t>(bytes));
+    ka = kz;
+  }
+  bulk_commit();
 }
 
 // kHashed: the change test is the 128-bit block hash against the HashCache
@@ -262,6 +387,7 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
     sh.ticket = t;
     sh.epoch = launch % 0xffffffffu + 1u;  // 1 .. 2^32-1: a zero-filled word never matches
     sh.bad = 0;
+    sh.ahead = 0;
   }
   // the launch must provide the flag words (and the staging of staged
   // tiles); if it does not, report it instead of touching memory past it
@@ -308,10 +434,29 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
       bulk_g2s(ws, w, 2u * te, &bar);
       bulk_g2s(cs, c, te, &bar);
     }
+    // Raw-ahead: a shard whose last payload was RAW (or any shard of a cold
+    // call, which is RAW by definition) is predicted raw again.  Its tiles
+    // store their values at their raw positions as soon as they arrive and
+    // skip the look-back; the shard's last tile checks the prediction.  Only
+    // shards whose every tile is staged take part.
+    sh.ahead = p.raw_ahead && (x.len & 15) == 0 && (cold || __ldg(p.pred + x.rl) != 0u);
   }
   __syncthreads();
 
-  if (warp == 0) {
+  if (warp == 0 && sh.ahead) {
+    if (lane == 0) {
+      if (mbar_wait_bounded(&bar, 0, p.timeout_ns)) {
+        int64_t off = 2 * x.e0;
+        if (kChecked && (p.flags & CIERA_DEBUG_OUT_OF_RANGE)) off += int64_t(1) << 40;
+        if (in_bounds(p.ctl, off, 2 * x.te, p.stride))
+          bulk_s2g(p.payloads + static_cast<int64_t>(x.rl) * p.stride + off, ws, 2u * te);
+        bulk_commit();
+      } else {
+        record_status(p.ctl, kStatusTimeout);
+        mbar_wait_bounded(&bar, 0, p.timeout_ns);
+      }
+    }
+  } else if (warp == 0) {
     bool to = false;
     const uint32_t X = lookback_exclusive(p, x, sh.epoch, lane, x.k0, &to);
     if (lane == 0) {
@@ -478,7 +623,7 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
             if (cold || ((e.x ^ cc.x) | (e.y ^ cc.y) | (e.z ^ cc.z) | (e.w ^ cc.w)))
               reinterpret_cast<uint4*>(c)[gi] = e;
           }
-        } else {
+        } else if (!sh.ahead) {
           reinterpret_cast<uint4*>(cs)[gi] =
               make_uint4(sm4(w0.x, w0.y), sm4(w0.z, w0.w), sm4(w1.x, w1.y), sm4(w1.z, w1.w));
         }
@@ -487,29 +632,17 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
     }
   }
   __syncthreads();
+  if (sh.ahead) {
+    if (x.t == x.tiles - 1) raw_ahead_finish(p, x, sh, fw);
+    if (tid == 0) bulk_wait_read_all();
+    return;
+  }
   if (tid == 0 && x.t > 0) publish(p, x, sh.epoch, kStateInclusive, sh.X + sh.agg);
 
   uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
   if (stg) {
     // the bulk stores are the only step that needs the prefix
-    if (tid == 0) {
-      int ka = 0;
-      while (ka < x.nblk) {
-        const bool f = flag_of(fw, ka);
-        int kz = ka + 1;
-        while (kz < x.nblk && flag_of(fw, kz) == f) ++kz;
-        const int64_t ea = static_cast<int64_t>(ka) * B;
-        const int64_t ez =
-            static_cast<int64_t>(kz) * B < x.te ? static_cast<int64_t>(kz) * B : x.te;
-        int64_t off = (x.k0 + ka + sh.X + count_before(fw, fpre, ka)) * B;
-        if (kChecked && (p.flags & CIERA_DEBUG_OUT_OF_RANGE)) off += int64_t(1) << 40;
-        const int64_t bytes = (f ? 2 : 1) * (ez - ea);
-        if (in_bounds(p.ctl, off, bytes, p.stride))
-          bulk_s2g(payload + off, f ? ws + 2 * ea : cs + ea, static_cast<uint32_t>(bytes));
-        ka = kz;
-      }
-      bulk_commit();
-    }
+    if (tid == 0) store_runs(p, x, fw, fpre, sh.X, ws, cs);
   } else {
     for (int64_t j = tid; j < x.te; j += blockDim.x) {
       const int kb = static_cast<int>(j / B);
@@ -549,6 +682,124 @@ __global__ void __launch_bounds__(kThreads) k_raw_fixup(const CompressParams p) 
     if (!in_bounds(p.ctl, o, 2, p.stride)) continue;
     payload[o] = static_cast<uint8_t>(v & 0xFFu);
     payload[o + 1] = static_cast<uint8_t>(v >> 8);
+  }
+}
+
+// After a k_compress launch with raw-ahead on: record each shard's outcome
+// as the next call's prediction, and rewrite in compacted layout every
+// raw-ahead shard that did not turn out raw.  Such a shard's last tile wrote
+// its descriptor and every tile's inclusive prefix; its tiles' flag words
+// carry the launch's tag.  CTA b rewrites tiles b, b + gridDim.x, ... of
+// each such shard from the values (the payload holds them at their raw
+// positions, which the compacted body overwrites), and the shard's last
+// tile appends the bitmap.  With nothing to rewrite every CTA exits after
+// reading the result words.
+// Dynamic shared memory: 128 bytes | ws[2*TE] values | cs[TE] sign+mantissa
+// bytes | one bit per shard (shards to rewrite).
+__global__ void __launch_bounds__(kThreads) k_repack(const CompressParams p) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ uint32_t s_epoch, s_nfix, s_X, s_bad;
+  __shared__ uint32_t s_fw[1], s_fpre[1];
+  __shared__ __align__(8) uint64_t bar;
+  const int tid = threadIdx.x;
+  const int64_t B = p.geo.B;
+  const int64_t TE = p.geo.T * B;
+  const int nr = p.geo.nfull + p.geo.has_part;  // shards with tiles
+  const int nmw = (nr + 31) / 32;
+  uint8_t* ws = dsm + 128;
+  uint8_t* cs = ws + 2 * TE;
+  uint32_t* mask = reinterpret_cast<uint32_t*>(cs + TE);
+  if (dynamic_smem_size() < static_cast<uint32_t>(128 + 3 * TE + 4 * nmw) || p.geo.T > 32) {
+    if (tid == 0) record_status(p.ctl, kStatusInternal);
+    return;
+  }
+  if (tid == 0) {
+    // the launch just finished drew its tag from the counter, then advanced it
+    const uint32_t launch = static_cast<uint32_t>(ld_relaxed_u64(&p.ctl->ticket) >> 32) - 1u;
+    s_epoch = launch % 0xffffffffu + 1u;
+    s_nfix = 0;
+    s_fpre[0] = 0;
+  }
+  for (int i = tid; i < nmw; i += kThreads) mask[i] = 0;
+  __syncthreads();
+  const uint32_t epoch = s_epoch;
+  for (int rl = tid; rl < nr; rl += kThreads) {
+    const unsigned long long v = p.result[rl];
+    const bool cur = (v >> 32) == epoch;
+    if (blockIdx.x == 0) p.pred[rl] = cur && (v & kResultRaw) ? 1u : 0u;
+    if (cur && (v & kResultRepack)) {
+      atomicOr(&mask[rl >> 5], 1u << (rl & 31));
+      atomicAdd(&s_nfix, 1u);
+    }
+  }
+  __syncthreads();
+  if (s_nfix == 0) return;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  uint32_t phase = 0;
+  const unsigned long long ep = static_cast<unsigned long long>(epoch);
+  for (int rl = 0; rl < nr; ++rl) {
+    if (!((mask[rl >> 5] >> (rl & 31)) & 1u)) continue;
+    const int64_t tiles = rl < p.geo.nfull ? p.geo.tiles_full : p.geo.tiles_part;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+      const Tile x = make_tile(p.geo, rl, t);
+      const uint32_t te = static_cast<uint32_t>(x.te);
+      if (tid == 0) {
+        mbar_arrive_expect_tx(&bar, 2u * te);
+        bulk_g2s(ws, p.w + x.shard_off + x.e0, 2u * te, &bar);
+        const unsigned long long f = ld_relaxed_u64(&p.tile_flags[x.sidx]);
+        const unsigned long long q = t > 0 ? ld_relaxed_u64(&p.tile_status[x.sidx - 1])
+                                           : (ep << 32) | (uint64_t(kStateInclusive) << 30);
+        s_fw[0] = static_cast<uint32_t>(f);
+        s_X = static_cast<uint32_t>(q & 0x3FFFFFFFull);
+        s_bad = (f >> 32) != ep || (q >> 32) != ep || ((q >> 30) & 3ull) != kStateInclusive ||
+                s_X > static_cast<uint32_t>(x.k0);
+        if (s_bad) record_status(p.ctl, kStatusInternal);
+      }
+      __syncthreads();
+      const bool ok = mbar_wait_bounded(&bar, phase, p.timeout_ns);
+      if (__syncthreads_or(!ok)) {
+        // wait once more so that no copy still writes into shared memory
+        // when the CTA exits
+        if (tid == 0) record_status(p.ctl, kStatusTimeout);
+        if (!ok) mbar_wait_bounded(&bar, phase, p.timeout_ns);
+        return;
+      }
+      phase ^= 1u;
+      const uint32_t fw0 = s_fw[0];
+      if (!s_bad) {
+        const int ngroups = static_cast<int>(te >> 4);
+        for (int gi = tid; gi < ngroups; gi += kThreads) {
+          const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
+          if ((fw0 >> kb) & 1u) continue;
+          const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
+          const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
+          reinterpret_cast<uint4*>(cs)[gi] =
+              make_uint4(sm4(w0.x, w0.y), sm4(w0.z, w0.w), sm4(w1.x, w1.y), sm4(w1.z, w1.w));
+        }
+        fence_proxy_async_smem();
+      }
+      __syncthreads();
+      if (!s_bad) {
+        if (tid == 0) store_runs(p, x, s_fw, s_fpre, s_X, ws, cs);
+        if (x.t == x.tiles - 1) {
+          const uint32_t total = s_X + __popc(fw0);
+          const bool last_changed = (fw0 >> (x.nb - 1 - x.k0)) & 1u;
+          const int64_t body = body_bytes_of(x, B, total, last_changed);
+          const int64_t bm = (x.nb + 7) / 8;
+          // the shard's last tile found it compressed, so body + bm < 2*len
+          if (body + bm < 2 * x.len)
+            write_bitmap(p, x, epoch, body, bm);
+          else if (tid == 0)
+            record_status(p.ctl, kStatusInternal);
+        }
+      }
+      if (tid == 0) bulk_wait_read_all();
+      __syncthreads();
+    }
   }
 }
 
@@ -832,6 +1083,28 @@ constexpr int kMaxDevices = 64;
 std::atomic<int64_t> g_compress_smem[kMaxDevices];
 std::atomic<int64_t> g_compress_hashed_smem[kMaxDevices];
 std::atomic<int64_t> g_decompress_smem[kMaxDevices];
+std::atomic<int64_t> g_repack_smem[kMaxDevices];
+std::atomic<int> g_sms[kMaxDevices];
+
+// Multiprocessors of the current device (looked up once per device).
+cudaError_t sm_count(int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < kMaxDevices) {
+    const int c = g_sms[dev].load(std::memory_order_relaxed);
+    if (c > 0) {
+      *out = c;
+      return cudaSuccess;
+    }
+  }
+  int n = 0;
+  e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (dev < kMaxDevices) g_sms[dev].store(n, std::memory_order_relaxed);
+  *out = n;
+  return cudaSuccess;
+}
 
 // Opt the kernel in to `bytes` of dynamic shared memory on the current
 // device (the default limit, static + dynamic, is 48 KB).
@@ -853,7 +1126,8 @@ cudaError_t allow_dynamic_smem(const void* fn, int64_t bytes, std::atomic<int64_
 
 }  // namespace
 
-int launch_compress(const CompressParams& p, int64_t smem_bytes, int raw_fixup, void* stream) {
+int launch_compress(const CompressParams& p, int64_t smem_bytes, int raw_fixup,
+                    int64_t repack_smem, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const void* fn = p.hashed ? reinterpret_cast<const void*>(k_compress<true>)
                             : reinterpret_cast<const void*>(k_compress<false>);
@@ -870,6 +1144,18 @@ int launch_compress(const CompressParams& p, int64_t smem_bytes, int raw_fixup, 
         <<<static_cast<unsigned>(grid), kThreads, static_cast<size_t>(smem_bytes), s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (p.raw_ahead && p.geo.total_tiles > 0) {
+    e = allow_dynamic_smem(reinterpret_cast<const void*>(k_repack), repack_smem, g_repack_smem);
+    if (e != cudaSuccess) return e;
+    int sms = 0;
+    e = sm_count(&sms);
+    if (e != cudaSuccess) return e;
+    const int64_t cap = 4 * static_cast<int64_t>(sms);
+    const int64_t grid = p.geo.total_tiles < cap ? p.geo.total_tiles : cap;
+    k_repack<<<static_cast<unsigned>(grid), kThreads, static_cast<size_t>(repack_smem), s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   if (raw_fixup && p.geo.total_tiles > 0) {
     k_raw_fixup<<<static_cast<unsigned>(p.geo.total_tiles), kThreads, 0, s>>>(p);
     e = cudaGetLastError();

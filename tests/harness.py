@@ -75,10 +75,12 @@ def compare_step(ag: SimulatedAllgather, ost: OracleState, w_np: np.ndarray, o_p
     np.testing.assert_array_equal(o_out, w_np, err_msg=f"{tag} oracle round trip")
 
 
-def run_parity(seq_np, ranks, block, device="cuda", tag=""):
-    """seq_np: list of uint16 numpy arrays (w_0, w_1, ...)."""
+def run_parity(seq_np, ranks, block, device="cuda", tag="", raw_ahead=True):
+    """seq_np: list of uint16 numpy arrays (w_0, w_1, ...).  raw_ahead=False
+    sends every shard through the look-back scan."""
     n = seq_np[0].size
-    ag = SimulatedAllgather(n, block, ranks, device=device, keep_flags=True)
+    ag = SimulatedAllgather(n, block, ranks, device=device, keep_flags=True,
+                            raw_ahead=raw_ahead)
     ost = OracleState(n, ranks, block)
     for t, w in enumerate(seq_np):
         w_dev = torch.from_numpy(w.view(np.int16)).to(device).view(torch.uint16)
@@ -88,3 +90,26 @@ def run_parity(seq_np, ranks, block, device="cuda", tag=""):
         o_payloads, o_descs, o_flags, o_out = ost.step(w)
         compare_step(ag, ost, w, o_payloads, o_descs, o_flags, o_out, tag=f"{tag} t={t}")
     return ag, ost
+
+
+def raw_ahead_sequence(n, ranks, block, iters=7, seed=0):
+    """Shard 0 changes every block every iteration (raw-ahead predicted right
+    after the cold start); shard 1 alternates between every block changed
+    and one changed value (predicted raw, then compacted: a rewrite every
+    other iteration); the remaining shards change sparsely."""
+    rng = np.random.default_rng(seed)
+    S = -(-n // ranks)
+    w = (rng.normal(0.0, 0.02, n).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    seq = [w.copy()]
+    for t in range(1, iters):
+        w = w.copy()
+        w[:S] ^= np.uint16(0x0080)
+        if t % 2:
+            w[S:2 * S] ^= np.uint16(0x0080)
+        else:
+            w[S + int(rng.integers(0, S))] ^= np.uint16(0x0080)
+        if ranks > 2:
+            idx = rng.integers(2 * S, n, max(1, (n - 2 * S) // 50000))
+            w[idx] ^= np.uint16(0x0100)
+        seq.append(w)
+    return seq

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from harness import eq16, to_np_u16, to_np_u8
+from harness import eq16, raw_ahead_sequence, to_np_u16, to_np_u8
 from lossless_exponent_reuse_gb300 import ciera, workloads
 from lossless_exponent_reuse_gb300.allgather import SimulatedAllgather
 
@@ -86,6 +86,12 @@ CASES = [
 def test_hashed_edge_sequences(n, ranks, block):
     run_hashed_parity(_sequence(n, block, n + block), ranks, block,
                       tag=f"n={n} R={ranks} B={block}")
+
+
+def test_hashed_raw_ahead_predictions_and_rewrites():
+    n, ranks, block = 4 * 65536, 4, 4096
+    run_hashed_parity(raw_ahead_sequence(n, ranks, block, seed=5), ranks, block,
+                      tag="raw-ahead hashed")
 
 
 def test_hashed_workload_1_and_clustered():

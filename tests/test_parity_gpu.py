@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from harness import eq16, exps_dev, run_parity
+from harness import eq16, exps_dev, raw_ahead_sequence, run_parity
 from lossless_exponent_reuse_gb300 import ciera, workloads
 from lossless_exponent_reuse_gb300.allgather import SimulatedAllgather
 
@@ -73,6 +73,29 @@ CASES = [
 def test_edge_sequences(n, ranks, block):
     run_parity(edge_sequence(n, block, seed=n + block), ranks, block,
                tag=f"n={n} R={ranks} B={block}")
+
+
+@pytest.mark.parametrize("n,ranks,block", [c for c in CASES if c[2] >= 256])
+def test_edge_sequences_look_back_only(n, ranks, block):
+    # the same sequences with raw-ahead off: every shard takes the look-back
+    run_parity(edge_sequence(n, block, seed=n + block), ranks, block,
+               tag=f"look-back n={n} R={ranks} B={block}", raw_ahead=False)
+
+
+@pytest.mark.parametrize("n,ranks,block", [
+    (4 * 65536, 4, 4096),       # 8 tiles per shard
+    (3 * 40960, 3, 256),        # 32-block tiles, 5 tiles per shard
+    (2 * 98304, 2, 16384),      # one block per tile
+    (81904, 20, 4096),          # partial last shard of 4080 values: raw-ahead too
+    (81914, 20, 4096),          # partial last shard of 4090 values: look-back, byte-wise
+])
+def test_raw_ahead_predictions_and_rewrites(n, ranks, block):
+    seq = raw_ahead_sequence(n, ranks, block, seed=n)
+    ag, _ = run_parity(seq, ranks, block, tag=f"raw-ahead n={n} B={block}")
+    d = ag.descriptors()
+    assert d[0]["mode"] == ciera.MODE_RAW
+    if ag.plan.info.blocks_per_shard > 1:              # the last iteration is even
+        assert d[1]["mode"] == ciera.MODE_COMPRESSED
 
 
 def test_raw_payload_with_one_unchanged_block():
@@ -148,15 +171,19 @@ def test_corrupt_descriptor_is_reported_and_skipped():
     assert ag.status() == ciera.OK                                  # cleared
 
 
-def test_bounded_wait_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("raw_ahead", [True, False])
+def test_bounded_wait_reports_timeout_and_context_survives(raw_ahead):
+    # a cold call is raw-ahead: the shard's last tile waits for tile 0's
+    # aggregate; without raw-ahead every later tile's look-back waits for it
     n, R, B = 4 * 4096 * 8, 4, 4096                                # 8 tiles per shard
     rng = np.random.default_rng(11)
     w = torch.from_numpy(_bf16(rng, n).view(np.int16)).cuda().view(torch.uint16)
     ag = SimulatedAllgather(n, B, R)
     ciera.set_wait_timeout_ns(2_000_000)
     try:
+        extra = ciera.DEBUG_SKIP_FIRST_PUBLISH | (0 if raw_ahead else ciera.NO_RAW_AHEAD)
         ag.plan.compress(w, ag.sender_cache, ag.payloads, ag.descs, ag.workspace, cold=True,
-                         extra_flags=ciera.DEBUG_SKIP_FIRST_PUBLISH)
+                         extra_flags=extra)
         assert ag.status() == ciera.E_TIMEOUT
     finally:
         ciera.set_wait_timeout_ns(1_000_000_000)
