@@ -586,9 +586,13 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
         const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
         const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
         const uint4 cc = reinterpret_cast<const uint4*>(cs)[gi];
-        const uint32_t d = (exp4(w0.x, w0.y) ^ cc.x) | (exp4(w0.z, w0.w) ^ cc.y) |
-                           (exp4(w1.x, w1.y) ^ cc.z) | (exp4(w1.z, w1.w) ^ cc.w);
-        if (d) {
+        const uint4 e = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w), exp4(w1.x, w1.y),
+                                   exp4(w1.z, w1.w));
+        if ((e.x ^ cc.x) | (e.y ^ cc.y) | (e.z ^ cc.z) | (e.w ^ cc.w)) {
+          // a group whose exponents differ lies in a changed block, and these
+          // are the only groups of changed blocks whose cache entry moves:
+          // refresh it here instead of in a second pass
+          reinterpret_cast<uint4*>(c)[gi] = e;
           const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
           atomicOr(&fw[kb >> 5], 1u << (kb & 31));
         }
@@ -603,30 +607,27 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
     }
     flaggers_sync();
     publish_aggregate(p, x, sh, sh, fw, fpre);
-    if (stg) {
+    // Without a compare (cold call, or a timed-out copy) every cache group
+    // of the tile is rewritten here; otherwise the compare refreshed them.
+    const bool refresh_all = !kHashed && (cold || sh.bad);
+    if (stg && (refresh_all || !sh.ahead)) {
       // Pack while warp 0 may still be looking back: nothing here depends
       // on the prefix.  Sign+mantissa bytes of an unchanged block overwrite
-      // its own cached exponents in cs (a group either reads cs -- changed
-      // block -- or writes it -- unchanged block -- never both).  Changed
-      // blocks refresh the sender cache, writing only the 16-byte groups
-      // that differ.
+      // its own cached exponents in cs, which nothing reads any more.  A
+      // raw-ahead tile sends its values as they are and packs nothing.
       const int ngroups = static_cast<int>(te >> 4);
       for (int gi = ft; gi < ngroups; gi += kThreads - 32) {
         const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
+        const bool f = flag_of(fw, kb);
+        if (f ? !refresh_all : sh.ahead) continue;
         const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
         const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
-        if (flag_of(fw, kb)) {
-          if (!kHashed) {
-            const uint4 e = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w), exp4(w1.x, w1.y),
-                                       exp4(w1.z, w1.w));
-            const uint4 cc = reinterpret_cast<const uint4*>(cs)[gi];
-            if (cold || ((e.x ^ cc.x) | (e.y ^ cc.y) | (e.z ^ cc.z) | (e.w ^ cc.w)))
-              reinterpret_cast<uint4*>(c)[gi] = e;
-          }
-        } else if (!sh.ahead) {
+        if (f)
+          reinterpret_cast<uint4*>(c)[gi] = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w),
+                                                       exp4(w1.x, w1.y), exp4(w1.z, w1.w));
+        else
           reinterpret_cast<uint4*>(cs)[gi] =
               make_uint4(sm4(w0.x, w0.y), sm4(w0.z, w0.w), sm4(w1.x, w1.y), sm4(w1.z, w1.w));
-        }
       }
       fence_proxy_async_smem();
     }
@@ -713,6 +714,8 @@ __global__ void __launch_bounds__(kThreads) k_repack(const CompressParams p) {
     if (tid == 0) record_status(p.ctl, kStatusInternal);
     return;
   }
+  // the first result word is loaded alongside the launch counter
+  const unsigned long long v0 = tid < nr ? p.result[tid] : 0ull;
   if (tid == 0) {
     // the launch just finished drew its tag from the counter, then advanced it
     const uint32_t launch = static_cast<uint32_t>(ld_relaxed_u64(&p.ctl->ticket) >> 32) - 1u;
@@ -724,7 +727,7 @@ __global__ void __launch_bounds__(kThreads) k_repack(const CompressParams p) {
   __syncthreads();
   const uint32_t epoch = s_epoch;
   for (int rl = tid; rl < nr; rl += kThreads) {
-    const unsigned long long v = p.result[rl];
+    const unsigned long long v = rl == tid ? v0 : p.result[rl];
     const bool cur = (v >> 32) == epoch;
     if (blockIdx.x == 0) p.pred[rl] = cur && (v & kResultRaw) ? 1u : 0u;
     if (cur && (v & kResultRepack)) {
