@@ -39,8 +39,8 @@
 //   k_rans_dec_tables  one CTA per RANS rank: a slot -> (symbol, frequency,
 //                      bias) table of 4096 entries from the received
 //                      frequencies, so that a decoding step is one lookup.
-//   k_decompress_rans  one CTA per tile.  RAW rank: a bulk copy of the
-//                      values, then out and ExpCache.  RANS rank: bulk copies
+//   k_decompress_rans  one CTA per tile.  RAW rank: the values stream from
+//                      the payload to out and ExpCache.  RANS rank: bulk copies
 //                      of the sign+mantissa bytes and the records; the kept
 //                      blocks merge with their cached exponents; one warp per
 //                      changed block decodes it (slot table read through L1)
@@ -646,28 +646,16 @@ __global__ void __launch_bounds__(kThreads)
     return;
   }
   if (state == kRankRaw) {
-    // the tile's values in one bulk copy, then out and the ExpCache
-    const uint32_t te2 = 2u * static_cast<uint32_t>(x.te);
-    uint8_t* vs = dsm + kRansDecMeta;  // [2 TE]
-    if (tid == 0) {
-      mbar_init(&bar, 1);
-      fence_barrier_init();
-      mbar_arrive_expect_tx(&bar, te2);
-      if (in_bounds(p.ctl, 2 * x.e0, te2, p.stride))
-        bulk_g2s(vs, p.payloads + static_cast<int64_t>(x.rl) * p.stride + 2 * x.e0, te2, &bar);
-    }
-    __syncthreads();
-    if (__syncthreads_or(!mbar_wait_bounded(&bar, 0, p.timeout_ns))) {
-      if (tid == 0) atomicOr(&p.ctl->status, kStatusTimeout);
-      mbar_wait_bounded(&bar, 0, p.timeout_ns);
-      __syncthreads();
-      return;
-    }
+    // the tile's values streamed from the payload to out, their exponents to
+    // the ExpCache (nothing staged)
+    if (!in_bounds(p.ctl, 2 * x.e0, 2 * x.te, p.stride)) return;
+    const uint4* vs = reinterpret_cast<const uint4*>(
+        p.payloads + static_cast<int64_t>(x.rl) * p.stride + 2 * x.e0);
     uint4* out = reinterpret_cast<uint4*>(p.out + x.shard_off + x.e0);
     uint4* rc = reinterpret_cast<uint4*>(p.rcache + x.shard_off + x.e0);
     for (int gi = tid; gi < static_cast<int>(x.te >> 4); gi += nthreads) {
-      const uint4 w0 = reinterpret_cast<const uint4*>(vs)[2 * gi];
-      const uint4 w1 = reinterpret_cast<const uint4*>(vs)[2 * gi + 1];
+      const uint4 w0 = __ldcs(vs + 2 * gi);
+      const uint4 w1 = __ldcs(vs + 2 * gi + 1);
       out[2 * gi] = w0;
       out[2 * gi + 1] = w1;
       rc[gi] = make_uint4(exp4(w0.x, w0.y), exp4(w0.z, w0.w), exp4(w1.x, w1.y), exp4(w1.z, w1.w));
@@ -676,7 +664,7 @@ __global__ void __launch_bounds__(kThreads)
   }
   uint32_t* offs = reinterpret_cast<uint32_t*>(dsm + kDOffs);
   uint8_t* ss = dsm + kRansDecMeta;   // sign+mantissa bytes [TE]
-  uint8_t* recs = ss + TE;            // the tile's records, when they fit [TE]
+  uint8_t* recs = ss + TE;            // the tile's records, when they fit [TE / 2]
   const ciera_desc d = p.descs[x.rl];
   const uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
   const RansLayout Ly = rans_layout(x.len, x.nb);
@@ -714,7 +702,7 @@ __global__ void __launch_bounds__(kThreads)
       rec_bytes += b - a;
     }
     // stage the records when they fit; else decode them from global memory
-    const bool staged = rec_bytes <= static_cast<uint64_t>(TE);
+    const bool staged = rec_bytes <= static_cast<uint64_t>(rans_record_stage(T, B));
     s_fw = fw;
     s_bad = bad;
     s_staged = staged;
