@@ -611,8 +611,37 @@ def run_e2e(wl, seq, n, K, dev, world, hashed=False, rans=False, raw_ahead=True)
         raise RuntimeError("e2e round trip is not exact")
     t = max_over_ranks(world, start.elapsed_time(end) / 1e3)
     val = 2.0 * sum_over_ranks(world, float(n * K)) / t / 1e9
+    link = link_bound(host, outs, hs, K, stream)
     return {"value": round(val, 2), "unit": UNIT, "h2d_bytes_per_step": 2 * n,
-            "d2h_bytes_per_step": 2 * n}
+            "d2h_bytes_per_step": 2 * n,
+            # the same bytes moved by plain copies alone, both directions at
+            # once on the same streams: what this machine's host link allows
+            "link_bound": round(link, 2)}
+
+
+def link_bound(host, outs, hs, K, stream):
+    """bf16 GB/s that the host link alone sustains for the e2e traffic: each
+    of K steps uploads one input (pinned) and downloads one output of the same
+    size, on the HostStreamer's two copy streams at the same time, with no
+    kernel in between.  The e2e figure divided by this is the share of the
+    link the path uses; boxes differ in this bound, the kernels do not."""
+    dev_in, dev_out = hs.w_buf, hs.out_buf
+    n = host[0].numel()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    hs.s_in.wait_stream(stream)
+    hs.s_out.wait_stream(stream)
+    for i in range(K):
+        with torch.cuda.stream(hs.s_in):
+            dev_in[i % 2][:n].copy_(host[i].view(torch.int16), non_blocking=True)
+        with torch.cuda.stream(hs.s_out):
+            outs[i % 2].copy_(dev_out[i % 2][:n], non_blocking=True)
+    stream.wait_stream(hs.s_in)
+    stream.wait_stream(hs.s_out)
+    end.record(stream)
+    torch.cuda.synchronize()
+    return 2.0 * n * K / (start.elapsed_time(end) / 1e3) / 1e9
 
 
 def run_reference(args, world, rank):
