@@ -27,7 +27,8 @@
 //                      frequency (Granlund and Montgomery, "Division by
 //                      invariant integers using multiplication", 1994), so
 //                      that a coding step multiplies instead of dividing.
-//   k_compress_rans    one CTA per tile, ticket order: one streaming pass
+//   k_compress_rans    one CTA per tile, ticket order: the tile's values and
+//                      cached exponents in bulk copies, one streaming pass
 //                      (flags by the exact test, cache refresh, sign+mantissa
 //                      bytes to their fixed positions, the tile's exponents
 //                      into shared memory, the sampled histogram); one warp
@@ -174,7 +175,7 @@ __device__ uint32_t rans_encode_block(const uint8_t* exps, int L, const uint4* t
   int top = LW;
   uint32_t x = kRansLow;
   const int n = L > lane ? (L - lane + kRansLanes - 1) / kRansLanes : 0;  // this lane's symbols
-#pragma unroll 8
+#pragma unroll 16
   for (int m = n - 1; m >= 0; --m) {
     const uint4 E = tab[exps[lane + kRansLanes * m]];
     // x >= f * 2^20: emit the low 16 bits.  The store is unconditional (a
@@ -268,11 +269,6 @@ __device__ bool rans_decode_block(const uint16_t* rec, uint32_t rec_words, int L
   return !__any_sync(0xffffffffu, idx != nw || x != kRansLow);
 }
 
-// Start pulling [src, src + bytes) into L2 (both 16-byte multiples).
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // One 16-value group of the sender's streaming pass (see k_compress_rans).
 __device__ __forceinline__ void stream_group(int gi, bool in, const uint4& w0, const uint4& w1,
                                              const uint4& cc, bool cold, bool direct_raw,
@@ -332,7 +328,9 @@ __global__ void __launch_bounds__(kThreads)
   uint32_t* red = reinterpret_cast<uint32_t*>(dsm + kCRed);
   uint32_t* fw = reinterpret_cast<uint32_t*>(dsm + kCFw);
   uint8_t* es = dsm + kRansEncMeta;  // the tile's exponents [TE]
-  uint8_t* scr = es + TE;            // one coding buffer per block [T * BB]
+  uint8_t* scr = es + TE;            // one coding buffer per block [T * BB], at first the
+                                     // tile's values (T * BB >= 2 * TE: a lane region
+                                     // holds more than two uint16 per value of its lane)
   const int64_t LW = rans_lane_words(B);
   const int64_t BB = rans_block_bytes(B);
 
@@ -378,15 +376,18 @@ __global__ void __launch_bounds__(kThreads)
   uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
   const uint32_t te = static_cast<uint32_t>(x.te);
   if (tid == 0) {
-    // the tile's values and cached exponents on their way into L2
-    bulk_prefetch_l2(w4, 2u * te);
-    bulk_prefetch_l2(c4, te);
-    // this shard's coder table (written by k_rans_enc_tables)
+    // This shard's coder table (written by k_rans_enc_tables), and the tile's
+    // values and cached exponents in two bulk copies.  The values land in the
+    // coding buffers and the cached exponents in the exponent region: both are
+    // free until the streaming pass has read them (the pass turns each group
+    // of cached exponents into the group's new exponents in place).
     mbar_init(&bar, 1);
     fence_barrier_init();
-    mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(kRansEncTableBytes));
+    mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(kRansEncTableBytes) + 3u * te);
     bulk_g2s(dsm + kCTab, enc_tables + kRansEncTableBytes * static_cast<int64_t>(x.rl),
              static_cast<uint32_t>(kRansEncTableBytes), &bar);
+    bulk_g2s(scr, w4, 2u * te, &bar);
+    bulk_g2s(es, c4, te, &bar);
   }
   __syncthreads();
 
@@ -408,25 +409,26 @@ __global__ void __launch_bounds__(kThreads)
     // the payload's bytes (sign+mantissa, or raw values), the exponents for
     // the coder, and the sampled histogram (the first value of each group).
     // The loop runs whole warps so that equal samples merge across lanes.
+    if (!mbar_wait_bounded(&bar, 0, p.timeout_ns)) {
+      record_status(p.ctl, kStatusTimeout);
+      mbar_wait_bounded(&bar, 0, p.timeout_ns);
+    }
     uint32_t mine = 0;
+    const uint4* ws4 = reinterpret_cast<const uint4*>(scr);
     for (int g0 = ft - lane; g0 < ngroups; g0 += kThreads - 32) {
       const int gi = g0 + lane;
       const bool in = gi < ngroups;
       uint4 w0 = {}, w1 = {}, cc = {};
       if (in) {
-        w0 = __ldg(w4 + 2 * gi);
-        w1 = __ldg(w4 + 2 * gi + 1);
-        cc = c4[gi];
+        w0 = ws4[2 * gi];
+        w1 = ws4[2 * gi + 1];
+        cc = reinterpret_cast<const uint4*>(es)[gi];
       }
       stream_group(gi, in, w0, w1, cc, cold, direct_raw, mG, c4, es, payload, x.e0, p.stride,
                    p.ctl, hist, mine, lane);
     }
     mine = __reduce_or_sync(0xffffffffu, mine);
     if (lane == 0 && mine) atomicOr(&fw[0], mine);
-    if (!mbar_wait_bounded(&bar, 0, p.timeout_ns)) {
-      record_status(p.ctl, kStatusTimeout);
-      mbar_wait_bounded(&bar, 0, p.timeout_ns);
-    }
     flaggers_sync();
     const uint32_t f = fw[0];
     // code the changed blocks: the i-th changed block goes to warp 1 + i % 3
