@@ -126,18 +126,23 @@ struct CompressShared {
   uint32_t red[kThreads / 32];  // per-warp sums of the raw-ahead finish
 };
 
-// Warps 1-3, after the flag bits are final: flag bytes, popcount prefix,
-// aggregate, and its publication (the inclusive prefix directly for a
-// shard's first tile).
-__device__ void publish_aggregate(const CompressParams& p, const Tile& x, const CompressShared& s0,
-                                  CompressShared& sh, uint32_t* fw, uint32_t* fpre) {
-  const int ft = threadIdx.x - 32;  // 0..95
+// Named barrier of the nf flagging threads of a compress CTA: warps 1-3
+// while warp 0 walks the look-back, all four warps on a raw-ahead tile.
+__device__ __forceinline__ void flag_sync(int nf) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nf) : "memory");
+}
+
+// The flagging threads (ft = 0 .. nf-1), after the flag bits are final: flag
+// bytes, popcount prefix, aggregate, and its publication (the inclusive
+// prefix directly for a shard's first tile).
+__device__ void publish_aggregate(const CompressParams& p, const Tile& x, CompressShared& sh,
+                                  uint32_t* fw, uint32_t* fpre, int ft, int nf) {
   const int nw = (x.nblk + 31) >> 5;
   uint8_t* fb = p.flagbytes + static_cast<int64_t>(x.rl) * p.flag_stride + x.k0;
   if (x.nblk > 32) {
-    for (int kb = ft; kb < x.nblk; kb += kThreads - 32) fb[kb] = flag_of(fw, kb) ? 1 : 0;
+    for (int kb = ft; kb < x.nblk; kb += nf) fb[kb] = flag_of(fw, kb) ? 1 : 0;
     if (ft < x.nblk) __threadfence();
-    flaggers_sync();
+    flag_sync(nf);
   }
   if (ft == 0) {
     // with flag bytes, the release of the status below orders these writes
@@ -158,7 +163,6 @@ __device__ void publish_aggregate(const CompressParams& p, const Tile& x, const 
     const uint32_t state = x.t == 0 && !sh.ahead ? kStateInclusive : kStateAggregate;
     if (!skip) publish(p, x, sh.epoch, state, run);
   }
-  (void)s0;
 }
 
 // Body size of a shard (len values, nb blocks) with `total` changed blocks;
@@ -355,8 +359,10 @@ __device__ void store_runs(const CompressParams& p, const Tile& x, const uint32_
 // (16 bytes per block) instead of an exponent compare against the sender's
 // exponent cache; then only the values are staged, and cs holds nothing but
 // the sign+mantissa bytes of unchanged blocks.  Needs T <= 32.
+// Nine CTAs fit an SM by shared memory (24.7 KB each); the bound keeps the
+// registers there too (without it the compiler picked 48 and spilled).
 template <bool kHashed>
-__global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
+__global__ void __launch_bounds__(kThreads, 9) k_compress(const CompressParams p) {
   extern __shared__ __align__(128) uint8_t dsm[];
   __shared__ CompressShared sh;
   __shared__ __align__(8) uint64_t bar;
@@ -448,20 +454,7 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
   }
   __syncthreads();
 
-  if (warp == 0 && sh.ahead) {
-    if (lane == 0) {
-      if (mbar_wait_bounded(&bar, 0, p.timeout_ns)) {
-        int64_t off = 2 * x.e0;
-        if (kChecked && (p.flags & CIERA_DEBUG_OUT_OF_RANGE)) off += int64_t(1) << 40;
-        if (in_bounds(p.ctl, off, 2 * x.te, p.stride))
-          bulk_s2g(p.payloads + static_cast<int64_t>(x.rl) * p.stride + off, ws, 2u * te);
-        bulk_commit();
-      } else {
-        record_status(p.ctl, kStatusTimeout);
-        mbar_wait_bounded(&bar, 0, p.timeout_ns);
-      }
-    }
-  } else if (warp == 0) {
+  if (warp == 0 && !sh.ahead) {
     bool to = false;
     const uint32_t X = lookback_exclusive(p, x, sh.epoch, lane, x.k0, &to);
     if (lane == 0) {
@@ -473,7 +466,11 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
     if (x.t == x.tiles - 1 && !flags_in_words(p)) __threadfence();
     if (stg) mbar_wait_bounded(&bar, 0, p.timeout_ns);  // this warp reads ws/cs too
   } else {
-    const int ft = tid - 32;
+    // the flagging threads: warps 1-3, or on a raw-ahead tile (no look-back)
+    // all four warps, whose thread 0 first stores the values at their raw
+    // positions
+    const int nf = sh.ahead ? kThreads : kThreads - 32;
+    const int ft = sh.ahead ? tid : tid - 32;
     if (stg) {
       if (!mbar_wait_bounded(&bar, 0, p.timeout_ns)) {
         // record it and wait once more, so no copy still writes into this
@@ -481,9 +478,15 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
         record_status(p.ctl, kStatusTimeout);
         sh.bad = 1;
         mbar_wait_bounded(&bar, 0, p.timeout_ns);
+      } else if (sh.ahead && tid == 0) {
+        int64_t off = 2 * x.e0;
+        if (kChecked && (p.flags & CIERA_DEBUG_OUT_OF_RANGE)) off += int64_t(1) << 40;
+        if (in_bounds(p.ctl, off, 2 * x.te, p.stride))
+          bulk_s2g(p.payloads + static_cast<int64_t>(x.rl) * p.stride + off, ws, 2u * te);
+        bulk_commit();
       }
     }
-    flaggers_sync();
+    flag_sync(nf);
     if (kHashed) {
       // per-block sums of the two seeds' word terms
       if (stg) {
@@ -510,7 +513,7 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
           s1 = s2 = 0;
           cur = -1;
         };
-        for (int g0 = ft - lane; g0 < ngroups; g0 += kThreads - 32) {
+        for (int g0 = ft - lane; g0 < ngroups; g0 += nf) {
           const int gi = g0 + lane;
           const bool in = gi < ngroups;
           int kb = -1;
@@ -550,7 +553,7 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
       } else {
         const int64_t wpb = (B + 7) / 8;  // exponent words per block
         const int64_t nwords = static_cast<int64_t>(x.nblk) * wpb;
-        for (int64_t q = ft; q < nwords; q += kThreads - 32) {
+        for (int64_t q = ft; q < nwords; q += nf) {
           const int kb = static_cast<int>(q / wpb);
           const int64_t j = q - kb * wpb;
           const int64_t first = kb * B + 8 * j;  // tile-relative
@@ -565,10 +568,10 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
           atomicAdd(&bsum[2 * kb + 1], t2);
         }
       }
-      flaggers_sync();
+      flag_sync(nf);
       // one thread per block: finish both hashes, test and refresh the
       // HashCache entry
-      for (int kb = ft; kb < x.nblk; kb += kThreads - 32) {
+      for (int kb = ft; kb < x.nblk; kb += nf) {
         const int64_t blen = (kb + 1) * B < x.te ? B : x.te - kb * B;
         const unsigned long long h1 = sm64_fin(static_cast<unsigned long long>(blen) + bsum[2 * kb]);
         const unsigned long long h2 =
@@ -584,10 +587,10 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
         }
       }
     } else if (cold || sh.bad) {
-      for (int kb = ft; kb < x.nblk; kb += kThreads - 32) atomicOr(&fw[kb >> 5], 1u << (kb & 31));
+      for (int kb = ft; kb < x.nblk; kb += nf) atomicOr(&fw[kb >> 5], 1u << (kb & 31));
     } else if (stg) {
       const int ngroups = static_cast<int>(te >> 4);
-      for (int gi = ft; gi < ngroups; gi += kThreads - 32) {
+      for (int gi = ft; gi < ngroups; gi += nf) {
         const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
         const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
         const uint4 cc = reinterpret_cast<const uint4*>(cs)[gi];
@@ -603,15 +606,15 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
         }
       }
     } else {
-      for (int64_t j = ft; j < x.te; j += kThreads - 32) {
+      for (int64_t j = ft; j < x.te; j += nf) {
         if (exp1(w[j]) != c[j]) {
           const int kb = static_cast<int>(j / B);
           atomicOr(&fw[kb >> 5], 1u << (kb & 31));
         }
       }
     }
-    flaggers_sync();
-    publish_aggregate(p, x, sh, sh, fw, fpre);
+    flag_sync(nf);
+    publish_aggregate(p, x, sh, fw, fpre, ft, nf);
     // Without a compare (cold call, or a timed-out copy) every cache group
     // of the tile is rewritten here; otherwise the compare refreshed them.
     const bool refresh_all = !kHashed && (cold || sh.bad);
@@ -621,7 +624,7 @@ __global__ void __launch_bounds__(kThreads) k_compress(const CompressParams p) {
       // its own cached exponents in cs, which nothing reads any more.  A
       // raw-ahead tile sends its values as they are and packs nothing.
       const int ngroups = static_cast<int>(te >> 4);
-      for (int gi = ft; gi < ngroups; gi += kThreads - 32) {
+      for (int gi = ft; gi < ngroups; gi += nf) {
         const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
         const bool f = flag_of(fw, kb);
         if (f ? !refresh_all : sh.ahead) continue;
