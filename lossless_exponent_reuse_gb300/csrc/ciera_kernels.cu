@@ -108,9 +108,9 @@ __device__ __forceinline__ void hash_word(unsigned long long word, int64_t j,
 //   then       warp 0 publishes the inclusive prefix, all warps pack, thread
 //              0 issues the bulk stores of the body, and the shard's last
 //              tile writes the descriptor and the bitmap.
-// A raw-ahead tile (its shard predicted RAW) skips the look-back: warp 0's
-// lane 0 stores the values at their raw positions as soon as they land, warps
-// 1-3 flag and refresh the cache, and the shard's last tile sums the
+// A raw-ahead tile (its shard predicted RAW) skips the look-back: thread 0
+// stores the values at their raw positions as soon as they land, all four
+// warps flag and refresh the cache, and the shard's last tile sums the
 // aggregates and checks the prediction (raw_ahead_finish; k_repack rewrites
 // the shard if it was wrong).
 // Dynamic shared memory: fw[W] flag words | fpre[W] their exclusive
