@@ -7,9 +7,11 @@
 // that must not grow its memory footprint mid-step, or plain C callers that
 // have no allocator of their own for a scratch buffer.  They still own and
 // pass every input and output; only the scratch (tile look-back words, the
-// ticket counter, the status word, per-block flag bytes) comes from
-// g_scratch below, which every GPU that loads this library holds until the
-// process exits.
+// ticket counter, the status word, per-block flag bytes, the per-rank
+// raw-ahead prediction and result words) comes from g_scratch below, which
+// every GPU that loads this library holds until the process exits.  Plans
+// that share the array share its predictions too; a stale prediction only
+// costs the rewrite of a shard, never its bytes.
 #include <cuda_runtime.h>
 
 #include <cstddef>
