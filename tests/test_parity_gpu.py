@@ -88,6 +88,7 @@ def test_edge_sequences_look_back_only(n, ranks, block):
     (2 * 98304, 2, 16384),      # one block per tile
     (81904, 20, 4096),          # partial last shard of 4080 values: raw-ahead too
     (81914, 20, 4096),          # partial last shard of 4090 values: look-back, byte-wise
+    (304, 20, 256),             # 16-value shards of one partial block, an empty last rank
 ])
 def test_raw_ahead_predictions_and_rewrites(n, ranks, block):
     seq = raw_ahead_sequence(n, ranks, block, seed=n)
