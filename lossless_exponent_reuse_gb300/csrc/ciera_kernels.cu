@@ -132,6 +132,18 @@ __device__ __forceinline__ void flag_sync(int nf) {
   asm volatile("bar.sync 1, %0;" ::"r"(nf) : "memory");
 }
 
+// Block of 16-value group gi on the staged paths (blocks of G = B/16 >= 16
+// groups, gi < 2^16): floor(gi / G) as mulhi(gi, m) with m = ceil(2^32 / G),
+// exact there because gi * (m - 2^32/G) / 2^32 < 2^-16 < 1/G.  A runtime
+// division per group was the largest item of the loops that use it.
+__device__ __forceinline__ uint32_t group_divisor(int64_t B) {
+  const uint32_t G = static_cast<uint32_t>(B >> 4);
+  return 0xffffffffu / G + 1u;  // = ceil(2^32 / G) for G >= 2
+}
+__device__ __forceinline__ int block_of_group(int gi, uint32_t m) {
+  return static_cast<int>(__umulhi(static_cast<uint32_t>(gi), m));
+}
+
 // The flagging threads (ft = 0 .. nf-1), after the flag bits are final: flag
 // bytes, popcount prefix, aggregate, and its publication (the inclusive
 // prefix directly for a shard's first tile).
@@ -427,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 9) k_compress(const CompressParams p
   }
   const Tile x = decode_ticket(p.geo, g);
   const bool stg = p.fast && (x.te & 15) == 0;
+  const uint32_t mG = stg ? group_divisor(B) : 0u;  // block_of_group (staged tiles)
   const bool cold = p.flags & CIERA_COLD;
   const uint16_t* w = p.w + x.shard_off + x.e0;
   uint8_t* c = p.scache + x.shard_off + x.e0;
@@ -521,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 9) k_compress(const CompressParams p
           if (in) {
             const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
             const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
-            kb = gi / G;
+            kb = block_of_group(gi, mG);
             const int64_t j0 = 2 * static_cast<int64_t>(gi - kb * G);  // first exponent word
             const unsigned long long lo =
                 exp4(w0.x, w0.y) | (static_cast<unsigned long long>(exp4(w0.z, w0.w)) << 32);
@@ -601,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 9) k_compress(const CompressParams p
           // are the only groups of changed blocks whose cache entry moves:
           // refresh it here instead of in a second pass
           reinterpret_cast<uint4*>(c)[gi] = e;
-          const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
+          const int kb = block_of_group(gi, mG);
           atomicOr(&fw[kb >> 5], 1u << (kb & 31));
         }
       }
@@ -625,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 9) k_compress(const CompressParams p
       // raw-ahead tile sends its values as they are and packs nothing.
       const int ngroups = static_cast<int>(te >> 4);
       for (int gi = ft; gi < ngroups; gi += nf) {
-        const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
+        const int kb = block_of_group(gi, mG);
         const bool f = flag_of(fw, kb);
         if (f ? !refresh_all : sh.ahead) continue;
         const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
@@ -751,6 +764,7 @@ __global__ void __launch_bounds__(kThreads) k_repack(const CompressParams p) {
   }
   __syncthreads();
   uint32_t phase = 0;
+  const uint32_t mG = group_divisor(B);
   const unsigned long long ep = static_cast<unsigned long long>(epoch);
   for (int rl = 0; rl < nr; ++rl) {
     if (!((mask[rl >> 5] >> (rl & 31)) & 1u)) continue;
@@ -784,7 +798,7 @@ __global__ void __launch_bounds__(kThreads) k_repack(const CompressParams p) {
       if (!s_bad) {
         const int ngroups = static_cast<int>(te >> 4);
         for (int gi = tid; gi < ngroups; gi += kThreads) {
-          const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
+          const int kb = block_of_group(gi, mG);
           if ((fw0 >> kb) & 1u) continue;
           const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
           const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
@@ -1047,8 +1061,9 @@ __device__ void decompress_tile_staged(const DecompressParams& p, const Tile& x,
   }
   const uint32_t fw = sh.fw[0];
   const int ngroups = static_cast<int>(te >> 4);
+  const uint32_t mG = group_divisor(B);
   for (int gi = tid; gi < ngroups; gi += blockDim.x) {
-    const int kb = static_cast<int>((static_cast<int64_t>(gi) << 4) / B);
+    const int kb = block_of_group(gi, mG);
     if (raw || ((fw >> kb) & 1u)) {
       const uint4 w0 = reinterpret_cast<const uint4*>(ws)[2 * gi];
       const uint4 w1 = reinterpret_cast<const uint4*>(ws)[2 * gi + 1];
