@@ -290,11 +290,13 @@ int ciera_compress_noalloc(ciera_plan_t plan, int rank_begin, int rank_count,
  * sender work of layer i+1 overlaps the receiver work of layer i.
  *
  * One layer of a step: the arguments of ciera_compress (all ranks) — or of
- * ciera_compress_rans, with `sender` = CIERA_SENDER_RANS — and of
+ * ciera_compress_rans, with `sender` = CIERA_SENDER_RANS, or of
+ * ciera_compress_hashed, with `sender` = CIERA_SENDER_HASHED — and of
  * ciera_decompress for that layer's plan.  A layer's compress and
  * decompress may share one workspace; different layers must not. */
 #define CIERA_SENDER_EXACT 0u
 #define CIERA_SENDER_RANS 1u
+#define CIERA_SENDER_HASHED 2u
 typedef struct {
     ciera_plan_t plan;
     const uint16_t *w_dev;         /* all ranks' values (sender input) */
@@ -305,10 +307,12 @@ typedef struct {
     uint8_t *recv_cache_dev;       /* ExpCache, N bytes */
     uint16_t *out_dev;             /* rebuilt values, N */
     void *workspace_dev;
-    uint32_t flags;                /* compress flags of this layer (CIERA_COLD) */
-    uint32_t sender;               /* CIERA_SENDER_EXACT or CIERA_SENDER_RANS */
+    uint32_t flags;                /* compress flags of this layer (CIERA_COLD, CIERA_NO_RAW_AHEAD) */
+    uint32_t sender;               /* CIERA_SENDER_EXACT, _RANS or _HASHED */
     const uint32_t *hist_prev_dev; /* RANS: hist_prev of ciera_compress_rans (else unused) */
     uint32_t *hist_out_dev;        /* RANS: its hist_out */
+    uint64_t *hash_cache_dev;      /* HASHED: the HashCache of ciera_compress_hashed (else
+                                      unused; sender_cache_dev is then unused) */
 } ciera_layer;
 
 typedef struct ciera_pipeline_s *ciera_pipeline_t;

@@ -38,6 +38,7 @@ NO_RAW_AHEAD = 2  # compress: every shard takes the look-back scan
 DECOMPRESS_RANS = 1
 SENDER_EXACT = 0
 SENDER_RANS = 1
+SENDER_HASHED = 2
 DEBUG_SKIP_FIRST_PUBLISH = 0x80000000
 DEBUG_OUT_OF_RANGE = 0x40000000  # accepted by checked builds only
 
@@ -64,7 +65,7 @@ class _Layer(ctypes.Structure):
                 ("recv_cache_dev", ctypes.c_void_p), ("out_dev", ctypes.c_void_p),
                 ("workspace_dev", ctypes.c_void_p), ("flags", ctypes.c_uint32),
                 ("sender", ctypes.c_uint32), ("hist_prev_dev", ctypes.c_void_p),
-                ("hist_out_dev", ctypes.c_void_p)]
+                ("hist_out_dev", ctypes.c_void_p), ("hash_cache_dev", ctypes.c_void_p)]
 
 
 class _CostModel(ctypes.Structure):
@@ -398,16 +399,17 @@ class Pipeline:
             self._h = None
 
     def step(self, layers, inputs, stream=None) -> None:
-        """layers: SimulatedAllgather objects (exact or RANS sender); inputs:
-        their weights for this step.  Advances each layer's iteration count."""
+        """layers: SimulatedAllgather objects (any sender); inputs: their
+        weights for this step.  Advances each layer's iteration count."""
         arr = (_Layer * len(layers))()
         for i, (ag, w) in enumerate(zip(layers, inputs)):
-            if ag.hashed:
-                raise ValueError("the pipeline drives the exact and the RANS senders")
-            hp = ho = None
+            hp = ho = hc = None
             if ag.rans:
                 hp = _dev_ptr(ag.hist[ag.iteration % 2], "hist_prev", torch.int32)
                 ho = _dev_ptr(ag.hist[(ag.iteration + 1) % 2], "hist_out", torch.int32)
+            if ag.hashed:
+                hc = _dev_ptr(ag.hash_cache, "hash_cache")
+            sender = SENDER_RANS if ag.rans else SENDER_HASHED if ag.hashed else SENDER_EXACT
             arr[i] = _Layer(ag.plan.handle.value, _dev_ptr(w, "w", torch.uint16),
                             _dev_ptr(ag.sender_cache, "sender_cache", torch.uint8),
                             _dev_ptr(ag.payloads, "payloads", torch.uint8),
@@ -416,7 +418,7 @@ class Pipeline:
                             _dev_ptr(ag.out, "out", torch.uint16),
                             _dev_ptr(ag.workspace, "workspace", torch.uint8),
                             (COLD if ag.iteration == 0 else 0) | ag.extra_flags,
-                            SENDER_RANS if ag.rans else SENDER_EXACT, hp, ho)
+                            sender, hp, ho, hc)
         _check(lib().ciera_pipeline_step(self._h, arr, len(layers), _stream_handle(stream),
                                          self.side.cuda_stream), "ciera_pipeline_step")
         for ag in layers:

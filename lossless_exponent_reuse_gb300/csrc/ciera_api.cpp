@@ -364,16 +364,22 @@ int ciera_pipeline_step(ciera_pipeline_t pp, const ciera_layer* layers, int n, v
     return CIERA_E_CUDA;
   for (int i = 0; i < n; ++i) {
     const ciera_layer& L = layers[i];
-    if (!L.plan || L.sender > CIERA_SENDER_RANS) return CIERA_E_INVAL;
+    if (!L.plan || L.sender > CIERA_SENDER_HASHED) return CIERA_E_INVAL;
     const bool rans = L.sender == CIERA_SENDER_RANS;
     const int ranks = static_cast<int>(L.plan->ranks);
-    int rc = rans ? ciera_compress_rans(L.plan, 0, ranks, L.w_dev, L.sender_cache_dev,
-                                        L.hist_prev_dev, L.hist_out_dev, L.payloads_dev,
-                                        L.payload_stride, L.descs_dev, nullptr, L.workspace_dev,
-                                        L.flags, side)
-                  : ciera_compress(L.plan, 0, ranks, L.w_dev, L.sender_cache_dev, L.payloads_dev,
-                                   L.payload_stride, L.descs_dev, nullptr, L.workspace_dev,
-                                   L.flags, side);
+    int rc;
+    if (rans)
+      rc = ciera_compress_rans(L.plan, 0, ranks, L.w_dev, L.sender_cache_dev, L.hist_prev_dev,
+                               L.hist_out_dev, L.payloads_dev, L.payload_stride, L.descs_dev,
+                               nullptr, L.workspace_dev, L.flags, side);
+    else if (L.sender == CIERA_SENDER_HASHED)
+      rc = ciera_compress_hashed(L.plan, 0, ranks, L.w_dev, L.hash_cache_dev, L.payloads_dev,
+                                 L.payload_stride, L.descs_dev, nullptr, L.workspace_dev,
+                                 L.flags, side);
+    else
+      rc = ciera_compress(L.plan, 0, ranks, L.w_dev, L.sender_cache_dev, L.payloads_dev,
+                          L.payload_stride, L.descs_dev, nullptr, L.workspace_dev, L.flags,
+                          side);
     if (rc != CIERA_OK) return rc;
     if (cudaEventRecord(pp->done[i], side) != cudaSuccess ||
         cudaStreamWaitEvent(s, pp->done[i], 0) != cudaSuccess)

@@ -106,3 +106,27 @@ def test_pipelined_rans_step_equals_layer_by_layer():
             assert torch.equal(b.out[:RANS_LAYERS[li][0]].view(torch.int16),
                                seqs[li][t].view(torch.int16))
     assert ciera.MODE_RANS in modes
+
+
+def test_pipelined_hashed_step_equals_layer_by_layer():
+    """The same with the hashed sender (Hash128 / HashCache) on every layer,
+    raw-ahead and look-back shards alike."""
+    seqs = _layer_seqs(4)
+    seq_layers = [SimulatedAllgather(n, B, R, hashed=True) for n, R, B in LAYERS]
+    pipe_layers = [SimulatedAllgather(n, B, R, hashed=True) for n, R, B in LAYERS]
+    pipe = ciera.Pipeline(len(LAYERS))
+    for t in range(4):
+        for ag, s in zip(seq_layers, seqs):
+            ag.step(s[t])
+        pipe.step(pipe_layers, [s[t] for s in seqs])
+        torch.cuda.synchronize()
+        for li, (a, b) in enumerate(zip(seq_layers, pipe_layers)):
+            assert b.status() == ciera.OK
+            assert a.descriptors() == b.descriptors(), (t, li)
+            for r, d in enumerate(a.descriptors()):
+                pb = d["payload_bytes"]
+                assert torch.equal(a.payloads[r, :pb], b.payloads[r, :pb]), (t, li, r)
+            assert torch.equal(a.hash_cache, b.hash_cache), (t, li)
+            assert torch.equal(a.recv_cache, b.recv_cache), (t, li)
+            assert torch.equal(b.out[:LAYERS[li][0]].view(torch.int16),
+                               seqs[li][t].view(torch.int16))
