@@ -32,9 +32,9 @@ def _sequence(n, block, seed):
     return [w0, w1, w2, w3]
 
 
-def run_hashed_parity(seq, ranks, block, tag=""):
+def run_hashed_parity(seq, ranks, block, tag="", raw_ahead=True):
     n = seq[0].size
-    ag = SimulatedAllgather(n, block, ranks, keep_flags=True, hashed=True)
+    ag = SimulatedAllgather(n, block, ranks, keep_flags=True, hashed=True, raw_ahead=raw_ahead)
     S = oracle.shard_size(n, ranks) if n else 0
     nb = oracle.num_blocks(S, block) if n else 0
     hc = np.zeros((ranks, max(nb, 1), 2), np.uint64)
