@@ -2,8 +2,8 @@
 computed offset is tested against its buffer, and one that would leave it is
 skipped and reported as CIERA_E_BOUNDS instead of touching memory.
 
-The GPU parity suites (small and full-size cases, graphs, the pipeline, the
-allocation-free entry point) run once more in a child process against the
+The GPU parity suites (small, random and full-size cases, graphs, the
+pipeline, the allocation-free entry point) run once more in a child process against the
 checked library (CIERA_CHECKED=1), which must give the same bytes and no
 status; the test hook CIERA_DEBUG_OUT_OF_RANGE, accepted only by the checked
 build, shows that the checks fire and that the library recovers."""
@@ -31,6 +31,7 @@ def test_parity_suites_under_the_checked_build():
         [sys.executable, "-m", "pytest", "-x", "-q", "-m", "gpu", "-p", "no:cacheprovider",
          "tests/test_parity_gpu.py", "tests/test_hashed_gpu.py", "tests/test_rans_gpu.py",
          "tests/test_fullsize_gpu.py", "tests/test_graph_gpu.py", "tests/test_pipeline_gpu.py",
+         "tests/test_random_gpu.py",
          "tests/test_checked_gpu.py::test_out_of_range_hook_is_caught",
          "tests/test_zz_no_alloc.py"],
         cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
