@@ -76,20 +76,21 @@ static_assert(kCFreq - kCTab + 512 == kRansEncTableBytes, "coder table layout");
 constexpr int kDOffs = 0;        // uint32[33] record-byte prefixes of the tile's blocks
 static_assert(kDOffs + 4 * 33 <= kRansDecMeta, "meta region");
 
-// Coder entry of a symbol of frequency f and cumulative frequency c:
-//   .x  m, the multiplier of floor(x / f) = (t + ((x - t) >> s1)) >> s2 with
-//       t = mulhi(x, m), l = ceil(log2 f), m = floor(2^32 (2^l - f) / f) + 1,
-//       s1 = min(l, 1), s2 = max(l - 1, 0)
-//   .y  f * 2^20, the bound at which the state emits 16 bits first
-//   .z  4096 - f
-//   .w  c | s1 << 16 | s2 << 24
+// Coder entry of a symbol of frequency f and cumulative frequency c, for a
+// coding step x -> x + q (4096 - f) + c with q = floor(x / f) (that is,
+// q * 4096 + (x - q f) + c):
+//   .x, .y  M = ceil(2^64 / f) as low and high words: for a state x < 2^32,
+//           q = floor((x M_hi + mulhi(x, M_lo)) / 2^32) exactly, because
+//           x (M - 2^64/f) / 2^64 < 2^-32 and x/f is at least 1/f short of
+//           the next integer.  For f = 1, M = 2^64 - 1 gives x - 1, and c
+//           carries the missing 4095 instead (4095 + c below).
+//   .z      f * 2^20, the bound at which the state emits 16 bits first
+//   .w      (4096 - f) | c << 16
 __device__ __forceinline__ uint4 coder_entry(uint32_t f, uint32_t c) {
-  const uint32_t l = 32u - __clz(f - 1u);  // ceil(log2 f); 0 for f = 1
-  const unsigned long long num = (1ull << 32) * ((1ull << l) - f);
-  const uint32_t m = static_cast<uint32_t>(num / f + 1ull);
-  const uint32_t s1 = l < 1u ? l : 1u;
-  const uint32_t s2 = l > 1u ? l - 1u : 0u;
-  return make_uint4(m, f << 20, kRansTotal - f, c | (s1 << 16) | (s2 << 24));
+  const unsigned long long M = f == 1u ? ~0ull : ~0ull / f + 1ull;
+  const uint32_t cc = f == 1u ? c + (kRansTotal - 1u) : c;
+  return make_uint4(static_cast<uint32_t>(M), static_cast<uint32_t>(M >> 32), f << 20,
+                    (kRansTotal - f) | (cc << 16));
 }
 
 // Block-wide reductions over the 256 threads of a table kernel.
@@ -180,13 +181,14 @@ __device__ uint32_t rans_encode_block(const uint8_t* exps, int L, const uint4* t
     const uint4 E = tab[exps[lane + kRansLanes * m]];
     // x >= f * 2^20: emit the low 16 bits.  The store is unconditional (a
     // word not emitted is overwritten by the next one); only top moves.
-    const bool emit = x >= E.y;
+    const bool emit = x >= E.z;
     region[top - 1] = static_cast<uint16_t>(x & 0xFFFFu);
     top -= emit ? 1 : 0;
     x = emit ? x >> 16 : x;
-    const uint32_t t = __umulhi(x, E.x);
-    const uint32_t q = (t + ((x - t) >> ((E.w >> 16) & 0xFFu))) >> (E.w >> 24);  // floor(x / f)
-    x += q * E.z + (E.w & 0xFFFFu);  // (q << 12) + x - q f + c
+    const unsigned long long xm =
+        static_cast<unsigned long long>(x) * E.y + __umulhi(x, E.x);
+    const uint32_t q = static_cast<uint32_t>(xm >> 32);  // floor(x / f) (x - 1 when f = 1)
+    x += q * (E.w & 0xFFFFu) + (E.w >> 16);              // (q << 12) + x - q f + c
   }
   region[--top] = static_cast<uint16_t>(x & 0xFFFFu);
   region[--top] = static_cast<uint16_t>(x >> 16);
