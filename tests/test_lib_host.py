@@ -179,3 +179,53 @@ def test_checked_build_compiles_and_exports_the_same_symbols():
     for name in declared_functions():
         assert hasattr(L, name), name
     assert L.ciera_strerror(ciera.E_BOUNDS) is not None
+
+
+def _c_layout(struct, fields):
+    """sizeof and offsetof of a header struct, from a C program built with gcc
+    against include/ciera.h (host compiler only; nothing runs on a GPU)."""
+    import subprocess
+    import tempfile
+    body = "".join(f'  printf("%zu\\n", offsetof({struct}, {f}));\n' for f in fields)
+    src = ("#include <stddef.h>\n#include <stdio.h>\n#include \"ciera.h\"\n"
+           f"int main(void) {{\n  printf(\"%zu\\n\", sizeof({struct}));\n{body}  return 0;\n}}\n")
+    with tempfile.TemporaryDirectory() as d:
+        c, exe = os.path.join(d, "l.c"), os.path.join(d, "l")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-std=c99", "-I", os.path.dirname(HEADER), c, "-o", exe],
+                       check=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout.split()
+    return int(out[0]), [int(v) for v in out[1:]]
+
+
+@pytest.mark.parametrize("struct,cls", [("ciera_plan_info_t", ciera._Info),
+                                        ("ciera_layer", ciera._Layer),
+                                        ("ciera_cost_model", ciera._CostModel)])
+def test_binding_struct_layouts_match_the_header(struct, cls):
+    fields = [f for f, _ in cls._fields_]
+    size, offsets = _c_layout(struct, fields)
+    assert ctypes.sizeof(cls) == size, struct
+    assert [getattr(cls, f).offset for f in fields] == offsets, struct
+
+
+def test_descriptor_is_24_bytes():
+    size, offsets = _c_layout("ciera_desc", ["mode", "n_changed_blocks", "body_bytes",
+                                             "payload_bytes"])
+    assert size == ciera.DESC_BYTES and offsets == [0, 4, 8, 16]
+
+
+def test_no_raw_ahead_is_a_known_compress_flag():
+    # unknown flags are refused before anything is launched; this one is not
+    # refused as unknown, so the call goes on to CUDA, which fails here for
+    # want of a device.  With a GPU the fake pointers would reach a kernel:
+    # there the test does not run.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("needs a machine without a GPU (fake device pointers)")
+    L = ciera.lib()
+    p = ciera.Plan(1024, 256, 4)
+    cap = p.info.payload_capacity
+    fake = ctypes.c_void_p(4096)
+    rc = L.ciera_compress(p.handle, 0, 4, fake, fake, fake, cap, fake, None, fake,
+                          ciera.NO_RAW_AHEAD, None)
+    assert rc == ciera.E_CUDA
