@@ -44,8 +44,8 @@
 //                      the payload to out and ExpCache.  RANS rank: bulk copies
 //                      of the sign+mantissa bytes and the records; the kept
 //                      blocks merge with their cached exponents; one warp per
-//                      changed block decodes it (slot table read through L1)
-//                      straight into the output and the ExpCache.
+//                      changed block decodes it (slot table copied into shared
+//                      memory) straight into the output and the ExpCache.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -207,18 +207,19 @@ __device__ uint32_t rans_encode_block(const uint8_t* exps, int L, const uint4* t
   return (kRansLanes + total + 7u) / 8u;
 }
 
-// One decoding step of a lane: symbol from the slot table, value and
+// One decoding step of a lane: symbol from the slot table (in shared
+// memory), value and
 // exponent out, state update, and a renormalisation that reads the word
 // loaded one step ahead (branch-free; the index is clamped to the lane's
 // last word, an overrun shows in the final check).
-__device__ __forceinline__ void decode_step(const uint32_t* __restrict__ tab, const uint16_t* s,
+__device__ __forceinline__ void decode_step(const uint32_t* tab, const uint16_t* s,
                                             uint32_t last, const uint8_t* sp, uint16_t* op,
                                             uint8_t* rp, uint32_t& x, uint32_t& idx,
                                             uint32_t& nxt) {
-  const uint32_t e = __ldg(tab + (x & (kRansTotal - 1)));
-  *op = static_cast<uint16_t>(join1(*sp, e & 0xFFu));
-  *rp = static_cast<uint8_t>(e);
-  x = ((e >> 8) & 0xFFFu) * (x >> kRansBits) + (e >> 20);
+  const uint32_t e = tab[x & (kRansTotal - 1)];
+  *op = static_cast<uint16_t>(join1(*sp, e >> 12));  // join1 keeps the low 8 bits
+  *rp = static_cast<uint8_t>(e >> 12);
+  x = (e >> 20) * (x >> kRansBits) + (e & 0xFFFu);  // f (x >> 12) + slot - cum
   const bool renorm = x < kRansLow;
   x = renorm ? (x << 16) | nxt : x;
   idx += renorm ? 1u : 0u;
@@ -226,12 +227,13 @@ __device__ __forceinline__ void decode_step(const uint32_t* __restrict__ tab, co
 }
 
 // One warp decodes one record of `rec_words` words into the block's L
-// exponents with the slot table `tab` (entry: symbol | f << 8 | (slot - cum)
-// << 20, read through L1), and writes each value (joined with its
+// exponents with the slot table `tab` (entry: (slot - cum) | symbol << 12 |
+// f << 20, so that f, on the state's critical path, takes one shift), and
+// writes each value (joined with its
 // sign+mantissa byte from `ss`) to `out` and its exponent to the ExpCache
 // `rc`.  False (for the whole warp) if the record does not decode cleanly.
 __device__ bool rans_decode_block(const uint16_t* rec, uint32_t rec_words, int L,
-                                  const uint32_t* __restrict__ tab, const uint8_t* ss,
+                                  const uint32_t* tab, const uint8_t* ss,
                                   uint16_t* out, uint8_t* rc, int lane) {
   const uint32_t nw = rec_words >= kRansLanes ? rec[lane] : 0u;
   uint32_t incl = nw;
@@ -621,7 +623,7 @@ __global__ void __launch_bounds__(kTableThreads)
   uint32_t sym = static_cast<uint32_t>(lo);
   for (uint32_t j = j0; j < j0 + 16; ++j) {
     while (sym < 255 && cum[sym + 1] <= j) ++sym;
-    out[j] = sym | ((cum[sym + 1] - cum[sym]) << 8) | ((j - cum[sym]) << 20);
+    out[j] = (j - cum[sym]) | (sym << 12) | ((cum[sym + 1] - cum[sym]) << 20);
   }
 }
 
@@ -669,6 +671,10 @@ __global__ void __launch_bounds__(kThreads)
   uint32_t* offs = reinterpret_cast<uint32_t*>(dsm + kDOffs);
   uint8_t* ss = dsm + kRansDecMeta;   // sign+mantissa bytes [TE]
   uint8_t* recs = ss + TE;            // the tile's records, when they fit [TE / 2]
+  // the rank's slot table, copied in with the tile: a decoding step is one
+  // dependent lookup in it, faster from shared memory than through L1
+  uint32_t* tabs =
+      reinterpret_cast<uint32_t*>(recs + ((rans_record_stage(T, B) + 15) & ~int64_t(15)));
   const ciera_desc d = p.descs[x.rl];
   const uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
   const RansLayout Ly = rans_layout(x.len, x.nb);
@@ -712,7 +718,10 @@ __global__ void __launch_bounds__(kThreads)
     s_staged = staged;
     mbar_init(&bar, 1);
     fence_barrier_init();
-    mbar_arrive_expect_tx(&bar, te + (staged ? static_cast<uint32_t>(rec_bytes) : 0u));
+    mbar_arrive_expect_tx(&bar, te + (staged ? static_cast<uint32_t>(rec_bytes) : 0u) +
+                                    static_cast<uint32_t>(kRansDecTableBytes));
+    bulk_g2s(tabs, dec_tables + 4096 * static_cast<int64_t>(x.rl),
+             static_cast<uint32_t>(kRansDecTableBytes), &bar);
     if (in_bounds(p.ctl, x.e0, te, p.stride)) bulk_g2s(ss, payload + x.e0, te, &bar);
     if (staged) {
       uint32_t at = 0;
@@ -761,7 +770,7 @@ __global__ void __launch_bounds__(kThreads)
   // decode the changed blocks straight into the output and the ExpCache:
   // the i-th changed block goes to warp i % 4
   const bool staged = s_staged;
-  const uint32_t* tab = dec_tables + 4096 * static_cast<int64_t>(x.rl);
+  const uint32_t* tab = tabs;
   bool ok = true;
   int i = 0;
   uint32_t at = 0;

@@ -35,8 +35,9 @@ constexpr int64_t kRansDecTableBytes = 4096 * 4;
 //   sender:   meta, the tile's exponents (T*B), one coding buffer per block
 //   receiver: meta, the tile's sign+mantissa bytes (T*B), its records when
 //             they fit in T*B/2 bytes (about 0.4 bytes per value at
-//             B = 4096; larger ones are decoded from global memory).  Raw
-//             tiles stream from global memory and stage nothing.
+//             B = 4096; larger ones are decoded from global memory), and the
+//             rank's 16 KB slot table.  Raw tiles stream from global memory
+//             and stage nothing.
 constexpr int64_t kRansEncMeta = 6144;  // coder table, histogram, sizes (ciera_rans.cu)
 constexpr int64_t kRansDecMeta = 1024;  // offsets
 __host__ __device__ inline int64_t rans_compress_smem(int64_t T, int64_t B) {
@@ -44,7 +45,8 @@ __host__ __device__ inline int64_t rans_compress_smem(int64_t T, int64_t B) {
 }
 __host__ __device__ inline int64_t rans_record_stage(int64_t T, int64_t B) { return T * B / 2; }
 __host__ __device__ inline int64_t rans_decompress_smem(int64_t T, int64_t B) {
-  return kRansDecMeta + T * B + rans_record_stage(T, B);
+  return kRansDecMeta + T * B + ((rans_record_stage(T, B) + 15) & ~int64_t(15)) +
+         kRansDecTableBytes;
 }
 // Threads of a receiver CTA.  (Two warps for tiles of two blocks, which
 // would idle no warp, were slower: more CTAs per SM leave less L1 for the
