@@ -71,6 +71,7 @@ constexpr int kCPre = 5760;      // uint32[33] exclusive prefix of the sizes
 constexpr int kCRed = 5904;      // uint32[8] reductions
 constexpr int kCFw = 5936;       // uint32 flag bits of the tile (T <= 32)
 static_assert(kCFw + 4 <= kRansEncMeta, "meta region");
+static_assert(kRansEncMeta >= 2 * kRansLanes, "the coder's look-ahead reads below the exponents");
 static_assert(kCFreq - kCTab + 512 == kRansEncTableBytes, "coder table layout");
 // ---- k_decompress_rans ---------------------------------------------------
 constexpr int kDOffs = 0;        // uint32[33] record-byte prefixes of the tile's blocks
@@ -176,9 +177,20 @@ __device__ uint32_t rans_encode_block(const uint8_t* exps, int L, const uint4* t
   int top = LW;
   uint32_t x = kRansLow;
   const int n = L > lane ? (L - lane + kRansLanes - 1) / kRansLanes : 0;  // this lane's symbols
+  // The next step's entry and the symbol two steps ahead are loaded before
+  // this step's store of a word, above which the compiler may not move them
+  // (all three live in shared memory).  Near the end the symbol index runs
+  // up to 64 bytes below the block's exponents: still inside the CTA's
+  // shared memory (the meta region precedes the exponents), and the entry
+  // loaded from it is never used.
+  const uint8_t* ep = exps + lane;
+  uint4 En = tab[ep[kRansLanes * (n - 1)]];
+  uint32_t sn = ep[kRansLanes * (n - 2)];
 #pragma unroll 16
   for (int m = n - 1; m >= 0; --m) {
-    const uint4 E = tab[exps[lane + kRansLanes * m]];
+    const uint4 E = En;
+    En = tab[sn];
+    sn = ep[kRansLanes * (m - 2)];
     // x >= f * 2^20: emit the low 16 bits.  The store is unconditional (a
     // word not emitted is overwritten by the next one); only top moves.
     const bool emit = x >= E.z;
