@@ -40,7 +40,8 @@
 //   k_rans_dec_tables  one CTA per RANS rank: a slot -> (symbol, frequency,
 //                      bias) table of 4096 entries from the received
 //                      frequencies, so that a decoding step is one lookup.
-//   k_decompress_rans  one CTA per tile.  RAW rank: the values stream from
+//   k_decompress_rans  one CTA per receiver tile (rans_receiver_blocks: twice
+//                      the sender's blocks).  RAW rank: the values stream from
 //                      the payload to out and ExpCache.  RANS rank: bulk copies
 //                      of the sign+mantissa bytes and the records; the kept
 //                      blocks merge with their cached exponents; one warp per
@@ -851,7 +852,21 @@ int launch_compress_rans(const CompressParams& p, const uint32_t* hist_prev, uin
   return e;
 }
 
-int launch_decompress_rans(const DecompressParams& p, uint32_t* dec_tables, void* stream) {
+// The geometry g with tiles of Tr blocks instead of g.T.
+static Geometry retiled(const Geometry& g, int64_t Tr) {
+  Geometry r = g;
+  r.T = Tr;
+  const int64_t nb_full = (g.S + g.B - 1) / g.B;
+  r.tiles_full = (nb_full + Tr - 1) / Tr;
+  r.tiles_part = g.has_part ? ((g.len_part + g.B - 1) / g.B + Tr - 1) / Tr : 0;
+  r.total_tiles = static_cast<int64_t>(g.nfull) * r.tiles_full + r.tiles_part;
+  return r;
+}
+
+int launch_decompress_rans(const DecompressParams& sender_tiles, uint32_t* dec_tables,
+                           void* stream) {
+  DecompressParams p = sender_tiles;
+  p.geo = retiled(sender_tiles.geo, rans_receiver_blocks(sender_tiles.geo.T));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p.geo.total_tiles <= 0) return cudaSuccess;
   const int64_t smem = rans_decompress_smem(p.geo.T, p.geo.B);

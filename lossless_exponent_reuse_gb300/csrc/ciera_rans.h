@@ -48,10 +48,17 @@ __host__ __device__ inline int64_t rans_decompress_smem(int64_t T, int64_t B) {
   return kRansDecMeta + T * B + ((rans_record_stage(T, B) + 15) & ~int64_t(15)) +
          kRansDecTableBytes;
 }
-// Threads of a receiver CTA.  (Two warps for tiles of two blocks, which
-// would idle no warp, were slower: more CTAs per SM leave less L1 for the
-// slot tables.)
+// Threads of a receiver CTA: four warps, each decoding one changed block at
+// a time.
 __host__ __device__ inline int rans_decompress_threads(int64_t) { return 128; }
+// Blocks per receiver tile for sender tiles of T blocks.  A payload
+// addresses its records per block, so the receiver may cut the shard into
+// tiles of its own: twice the sender's (at most 32) keeps all four warps
+// decoding on shards whose blocks all changed and loads the 16 KB slot
+// table once per four blocks instead of two.
+__host__ __device__ inline int64_t rans_receiver_blocks(int64_t T) {
+  return 2 * T > 32 ? 32 : 2 * T;
+}
 
 // Launchers (ciera_rans.cu), returning a cudaError_t value.
 //   launch_compress_rans: the RANS sender; hist_prev/hist_out hold 256

@@ -123,6 +123,7 @@ CASES = [
     (90048, 3, 4096),       # 2-block tiles, partial last block
     (98304, 3, 16384),      # one block per tile
     (65536, 2, 272),        # 30-block tiles, partial last block
+    (150400, 2, 1504),      # 5-block tiles; the receiver's 10-block tiles straddle bitmap words
     (131056, 32, 1024),     # 32 ranks, a short last shard
     (8176, 32, 256),        # tiny shards (always raw: sections alone reach 2*len)
     (76512, 300, 256),      # 300 ranks: a short shard and an empty one
