@@ -78,6 +78,11 @@ static_assert(kCFreq - kCTab + 512 == kRansEncTableBytes, "coder table layout");
 constexpr int kDOffs = 0;        // uint32[33] record-byte prefixes of the tile's blocks
 static_assert(kDOffs + 4 * 33 <= kRansDecMeta, "meta region");
 
+// Hint that the line holding p (global memory) be brought into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Coder entry of a symbol of frequency f and cumulative frequency c, for a
 // coding step x -> x + q (4096 - f) + c with q = floor(x / f) (that is,
 // q * 4096 + (x - q f) + c):
@@ -759,6 +764,12 @@ __global__ void __launch_bounds__(kThreads)
     if (gi < ngroups && !((fw >> __umulhi(static_cast<uint32_t>(gi), mG)) & 1u))
       kept[q] = reinterpret_cast<const uint4*>(rc)[gi];
   }
+  // the kept blocks' cached exponents beyond those groups, 128-byte lines
+  // wholly inside the tile, into L2 ahead of the merge (a receiver tile is
+  // twice the sender's, so these are half of it)
+  for (int li = kPer * nthreads / 8 + tid; li < static_cast<int>(te >> 7); li += nthreads)
+    if (!((fw >> __umulhi(static_cast<uint32_t>(8 * li), mG)) & 1u))
+      prefetch_l2(rc + 128 * static_cast<int64_t>(li));
   if (__syncthreads_or(!mbar_wait_bounded(&bar, 0, p.timeout_ns))) {
     if (tid == 0) atomicOr(&p.ctl->status, kStatusTimeout);
     mbar_wait_bounded(&bar, 0, p.timeout_ns);
