@@ -132,6 +132,17 @@ __device__ __forceinline__ void flag_sync(int nf) {
   asm volatile("bar.sync 1, %0;" ::"r"(nf) : "memory");
 }
 
+// A compress CTA sends to L2 the values and cached exponents of the tile
+// kPrefetchAhead tickets after its own (about a third of the CTAs resident on
+// the GPU), unless that tile's shard is predicted raw.  A tile that waits on
+// its look-back holds its staging, so fewer loads are in flight; the lines
+// brought in ahead keep DRAM busy meanwhile, and the later tile's bulk copies
+// find them in L2.  Much further ahead the lines are evicted before use.
+constexpr int64_t kPrefetchAhead = 512;
+__device__ __forceinline__ void prefetch_l2(const void* a) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
+
 // Block of 16-value group gi on the staged paths (blocks of G = B/16 >= 16
 // groups, gi < 2^16): floor(gi / G) as mulhi(gi, m) with m = ceil(2^32 / G),
 // exact there because gi * (m - 2^32/G) / 2^32 < 2^-16 < 1/G.  A runtime
@@ -466,6 +477,20 @@ __global__ void __launch_bounds__(kThreads, 9) k_compress(const CompressParams p
     sh.ahead = p.raw_ahead && (x.len & 15) == 0 && (cold || __ldg(p.pred + x.rl) != 0u);
   }
   __syncthreads();
+  if (!kHashed && stg && g + kPrefetchAhead < p.geo.total_tiles) {
+    const Tile y = decode_ticket(p.geo, g + kPrefetchAhead);
+    const bool y_ahead =
+        p.raw_ahead && (y.len & 15) == 0 && (cold || __ldg(p.pred + y.rl) != 0u);
+    if (!y_ahead) {
+      // 128-byte lines wholly inside the tile's values, then its cached exponents
+      const char* wy = reinterpret_cast<const char*>(p.w + y.shard_off + y.e0);
+      const char* cy = reinterpret_cast<const char*>(p.scache + y.shard_off + y.e0);
+      const int nw = static_cast<int>((2 * y.te) >> 7), nc = static_cast<int>(y.te >> 7);
+      for (int i = tid; i < nw + nc; i += blockDim.x)
+        prefetch_l2(i < nw ? wy + 128 * static_cast<int64_t>(i)
+                           : cy + 128 * static_cast<int64_t>(i - nw));
+    }
+  }
 
   if (warp == 0 && !sh.ahead) {
     bool to = false;
