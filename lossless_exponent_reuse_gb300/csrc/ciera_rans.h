@@ -65,7 +65,9 @@ __host__ __device__ inline int64_t rans_receiver_blocks(int64_t T) {
 //     uint32 per rank of the range (hist_out zeroed by the caller),
 //     enc_tables kRansEncTableBytes per rank of the range.
 //   launch_decompress_rans: the RANS part of the receiver, after the bitmap
-//     scan; dec_tables kRansDecTableBytes per rank.
+//     scan; dec_tables kRansDecTableBytes per rank.  p.geo is the plan's
+//     (the sender's) geometry; the launch re-tiles it to
+//     rans_receiver_blocks(p.geo.T) blocks per tile.
 int launch_compress_rans(const CompressParams& p, const uint32_t* hist_prev, uint32_t* hist_out,
                          uint8_t* enc_tables, void* stream);
 int launch_decompress_rans(const DecompressParams& p, uint32_t* dec_tables, void* stream);
