@@ -336,7 +336,8 @@ __device__ uint32_t lookback_exclusive(const CompressParams& p, const Tile& x, u
         }
         // back off: the status word is an L2 round trip away, and a
         // thousand CTAs polling at full rate slow everyone's loads
-        // (512 ns measured best among 32 .. 4096 on the OLMoE layer)
+        // (512 ns measured best among 32 .. 4096 on the OLMoE layer, and
+        // again against 128, 256 and 1024 once tiles prefetch ahead)
         __nanosleep(512);
       }
     }
