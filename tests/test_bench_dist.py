@@ -4,7 +4,6 @@ CPU.  No GPU is involved."""
 import os
 import socket
 
-import pytest
 import torch.multiprocessing as mp
 
 

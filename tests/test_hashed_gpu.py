@@ -2,7 +2,6 @@
 test, CIERA Section 3.1 and Appendix A, Algorithm 1) with the oracle, byte
 for byte: flags, descriptors, payloads, the HashCache, and the receiver's
 rebuilt values and ExpCache."""
-import ctypes
 
 import numpy as np
 import pytest

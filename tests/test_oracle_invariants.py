@@ -10,11 +10,9 @@ Section 3.2, Appendix A Algorithm 1; lossless reconstruction, Section 4.6):
   previous and the current weights (computed from the weights themselves);
 * exhaustive tiny cases over every subset of changed positions.
 """
-import itertools
 
 import numpy as np
 import pytest
-import torch
 
 import oracle
 from lossless_exponent_reuse_gb300 import workloads

@@ -10,7 +10,6 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
 from harness import eq16, exps_dev, raw_ahead_sequence, run_parity
 from lossless_exponent_reuse_gb300 import ciera, workloads
 from lossless_exponent_reuse_gb300.allgather import SimulatedAllgather

@@ -2,7 +2,6 @@
 compress(i+1) on a side stream overlapping decompress(i).  The pipelined
 step must equal layer-by-layer calls byte for byte, eagerly and when the
 step is captured into a CUDA graph and replayed."""
-import numpy as np
 import pytest
 import torch
 

@@ -8,7 +8,6 @@ run stopping at the first failure has already run every other test.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
