@@ -82,11 +82,6 @@ extern "C" {
  * that the tiles after it (for a raw-ahead shard: its last tile) run into
  * the bounded wait (CIERA_E_TIMEOUT). */
 #define CIERA_DEBUG_SKIP_FIRST_PUBLISH 0x80000000u
-/* Test hook of checked builds only (a library built with -DCIERA_CHECKED;
- * other builds reject the flag with CIERA_E_INVAL): ciera_compress moves
- * its payload stores 2^40 bytes out of range, so that the bounds checks
- * skip them and record CIERA_E_BOUNDS. */
-#define CIERA_DEBUG_OUT_OF_RANGE 0x40000000u
 
 typedef struct ciera_plan_s *ciera_plan_t;
 
@@ -262,6 +257,14 @@ int ciera_decompress(ciera_plan_t plan, const uint8_t *payloads_dev, int64_t pay
  * CIERA_E_BOUNDS (checked builds only) or CIERA_E_CUDA. */
 int ciera_status(void *workspace_dev, void *stream);
 
+/* Bits of a kernel status word (the status_dev output of
+ * ciera_compress_noalloc; ciera_status() maps the same bits of a workspace
+ * to its return codes). */
+#define CIERA_STATUS_CORRUPT 1u  /* receiver: a rank did not check out (CIERA_E_CORRUPT) */
+#define CIERA_STATUS_TIMEOUT 2u  /* a bounded wait ran out (CIERA_E_TIMEOUT) */
+#define CIERA_STATUS_INTERNAL 4u /* inconsistent launch configuration (CIERA_E_INTERNAL) */
+#define CIERA_STATUS_BOUNDS 8u   /* checked builds: an access was skipped (CIERA_E_BOUNDS) */
+
 /* Sender side without a workspace, for callers that cannot allocate device
  * memory where they compress (inside a communication hook or an allocator
  * callback, where allocating would re-enter the allocator; or C callers with
@@ -270,15 +273,19 @@ int ciera_status(void *workspace_dev, void *stream);
  * scratch (ticket counter, status word, look-back words, flag bytes) lives
  * in a fixed 8 MiB device array inside the library, which every GPU that
  * loads the library holds until the process exits.
- *   status_dev  optional (may be NULL): one device word the call sets to 0
- *               when its kernel finished normally, nonzero when a bounded
- *               wait ran out or the launch was inconsistent (the payloads of
- *               that call are then not valid)
+ *   status_dev  optional (may be NULL): one device word that receives the
+ *               call's kernel status bits: 0 when its kernels finished
+ *               normally, else an OR of CIERA_STATUS_TIMEOUT,
+ *               CIERA_STATUS_INTERNAL and (checked builds)
+ *               CIERA_STATUS_BOUNDS; the payloads of that call are then not
+ *               valid
  * It allocates nothing (no cudaMalloc, no allocating library routine).  Its
  * first call on a device looks up the array's device address; make that
  * first call before any stream capture.  Every call shares the one array:
  * calls that can overlap on the GPU (other streams, other host threads)
- * race and must be serialised by the caller.
+ * race and must be serialised by the caller.  Plans of different shapes may
+ * take turns: a call whose plan shape (numel, ranks, block) differs from the
+ * previous call's on the device first clears the scratch it uses.
  * Errors: CIERA_E_INVAL as ciera_compress, and for a plan whose
  * info.workspace_bytes exceeds 8 MiB; CIERA_E_CUDA. */
 int ciera_compress_noalloc(ciera_plan_t plan, int rank_begin, int rank_count,

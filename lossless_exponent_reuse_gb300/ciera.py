@@ -40,7 +40,6 @@ SENDER_EXACT = 0
 SENDER_RANS = 1
 SENDER_HASHED = 2
 DEBUG_SKIP_FIRST_PUBLISH = 0x80000000
-DEBUG_OUT_OF_RANGE = 0x40000000  # accepted by checked builds only
 
 DESC_BYTES = 24
 

@@ -20,14 +20,8 @@
 
 using namespace ciera;
 
-// Flags every compress entry point accepts; the out-of-range test hook only
-// in checked builds, where the kernels skip the accesses it provokes.
-#ifdef CIERA_CHECKED
-constexpr uint32_t kCompressFlags = CIERA_COLD | CIERA_NO_RAW_AHEAD |
-                                    CIERA_DEBUG_SKIP_FIRST_PUBLISH | CIERA_DEBUG_OUT_OF_RANGE;
-#else
+// Flags every compress entry point accepts.
 constexpr uint32_t kCompressFlags = CIERA_COLD | CIERA_NO_RAW_AHEAD | CIERA_DEBUG_SKIP_FIRST_PUBLISH;
-#endif
 
 struct ciera_plan_s {
   int64_t numel;

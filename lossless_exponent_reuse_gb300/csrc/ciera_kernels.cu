@@ -368,8 +368,7 @@ __device__ void store_runs(const CompressParams& p, const Tile& x, const uint32_
     while (kz < x.nblk && flag_of(fw, kz) == f) ++kz;
     const int64_t ea = static_cast<int64_t>(ka) * B;
     const int64_t ez = static_cast<int64_t>(kz) * B < x.te ? static_cast<int64_t>(kz) * B : x.te;
-    int64_t off = (x.k0 + ka + X + count_before(fw, fpre, ka)) * B;
-    if (kChecked && (p.flags & CIERA_DEBUG_OUT_OF_RANGE)) off += int64_t(1) << 40;
+    const int64_t off = (x.k0 + ka + X + count_before(fw, fpre, ka)) * B;
     const int64_t bytes = (f ? 2 : 1) * (ez - ea);
     if (in_bounds(p.ctl, off, bytes, p.stride))
       bulk_s2g(payload + off, f ? ws + 2 * ea : cs + ea, static_cast<uint32_t>(bytes));
@@ -518,8 +517,7 @@ __global__ void __launch_bounds__(kThreads, 9) k_compress(const CompressParams p
         mbar_wait_bounded(&bar, 0, p.timeout_ns);
       } else if (sh.ahead && tid == 0) {
         int64_t off = 2 * x.e0;
-        if (kChecked && (p.flags & CIERA_DEBUG_OUT_OF_RANGE)) off += int64_t(1) << 40;
-        if (in_bounds(p.ctl, off, 2 * x.te, p.stride))
+            if (in_bounds(p.ctl, off, 2 * x.te, p.stride))
           bulk_s2g(p.payloads + static_cast<int64_t>(x.rl) * p.stride + off, ws, 2u * te);
         bulk_commit();
       }
