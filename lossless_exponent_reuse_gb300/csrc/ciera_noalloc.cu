@@ -9,9 +9,18 @@
 // pass every input and output; only the scratch (tile look-back words, the
 // ticket counter, the status word, per-block flag bytes, the per-rank
 // raw-ahead prediction and result words) comes from g_scratch below, which
-// every GPU that loads this library holds until the process exits.  Plans
-// that share the array share its predictions too; a stale prediction only
-// costs the rewrite of a shard, never its bytes.
+// every GPU that loads this library holds until the process exits.
+//
+// Where a plan keeps each piece of scratch (look-back words, flag words, flag
+// bytes, predictions) depends on its size, rank count and block size.  A
+// call whose plan has another shape than the previous call's on the same
+// device would find the previous plan's bytes in its own regions -- for
+// instance flag bytes where it expects launch-tagged flag words, which could
+// read as a word of its own launch.  So the first call on a device, and
+// every call whose plan shape differs from the previous call's there, clears
+// the scratch the plan uses (all of it but the launch counter) before its
+// kernels run.  Calls of one plan shape reuse the scratch as a workspace is
+// reused.
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -29,13 +38,26 @@ constexpr size_t kScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
+
+// The plan shape that fixes the scratch layout (every offset of a workspace
+// follows from these three numbers).
+struct Shape {
+  int64_t numel = -1, ranks = -1, block = -1;
+  bool operator==(const Shape& o) const {
+    return numel == o.numel && ranks == o.ranks && block == o.block;
+  }
+};
+
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+Shape g_last_shape[kMaxDevices];  // shape of the last call on each device
 
-// Device address of g_scratch on the current device.  In host code the name
-// g_scratch is only a host-side stand-in, so the address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
-int scratch_address(void** out) {
+// Device address of g_scratch on the current device, and whether `shape`
+// differs from the previous call's on that device (recorded as the new last
+// shape).  In host code the name g_scratch is only a host-side stand-in, so
+// the address comes from cudaGetSymbolAddress, once per device, with that
+// device current.
+int scratch_address(const Shape& shape, void** out, bool* shape_changed) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CIERA_E_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -44,9 +66,19 @@ int scratch_address(void** out) {
     if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return CIERA_E_CUDA;
     g_scratch_ptr[dev] = p;
   }
+  *shape_changed = !(g_last_shape[dev] == shape);
+  g_last_shape[dev] = shape;
   *out = g_scratch_ptr[dev];
   return CIERA_OK;
 }
+
+static_assert(offsetof(ciera::Control, ticket) == 0 && sizeof(ciera::Control::ticket) == 8,
+              "the launch counter is the first 8 bytes of the scratch");
+static_assert(CIERA_STATUS_CORRUPT == ciera::kStatusCorrupt &&
+                  CIERA_STATUS_TIMEOUT == ciera::kStatusTimeout &&
+                  CIERA_STATUS_INTERNAL == ciera::kStatusInternal &&
+                  CIERA_STATUS_BOUNDS == ciera::kStatusBounds,
+              "status bits of the public header and of the kernels agree");
 
 }  // namespace
 
@@ -59,19 +91,26 @@ extern "C" int ciera_compress_noalloc(ciera_plan_t plan, int rank_begin, int ran
   if (ciera_plan_info(plan, &info) != CIERA_OK) return CIERA_E_INVAL;
   if (info.workspace_bytes > static_cast<int64_t>(kScratchBytes)) return CIERA_E_INVAL;
   void* scratch = nullptr;
-  const int st = scratch_address(&scratch);
+  bool shape_changed = false;
+  const int st =
+      scratch_address(Shape{info.numel, info.ranks, info.block}, &scratch, &shape_changed);
   if (st != CIERA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The array keeps the previous call's contents.  The ticket count (the
   // low half of the counter word) and the status word must start at zero;
   // the launch number in the counter's high half must be kept, because the
-  // look-back and flag words are tagged with it, and the flag bytes are
-  // rewritten before they are read.
+  // look-back and flag words are tagged with it.  After a change of plan
+  // shape everything past the counter is cleared as well: zero never
+  // matches a launch tag, and a zero prediction only sends a shard through
+  // the look-back.
   unsigned char* ctl = static_cast<unsigned char*>(scratch);
   if (cudaMemsetAsync(ctl + offsetof(ciera::Control, ticket), 0, sizeof(uint32_t), s) !=
-          cudaSuccess ||
-      cudaMemsetAsync(ctl + offsetof(ciera::Control, status), 0, sizeof(uint32_t), s) !=
-          cudaSuccess)
+      cudaSuccess)
+    return CIERA_E_CUDA;
+  const size_t clear_from = offsetof(ciera::Control, status);
+  const size_t clear_to =
+      shape_changed ? static_cast<size_t>(info.workspace_bytes) : clear_from + sizeof(uint32_t);
+  if (cudaMemsetAsync(ctl + clear_from, 0, clear_to - clear_from, s) != cudaSuccess)
     return CIERA_E_CUDA;
   const int rc = ciera_compress(plan, rank_begin, rank_count, w_dev, sender_cache_dev,
                                 payloads_dev, payload_stride, descs_dev, flags_dev, scratch,
