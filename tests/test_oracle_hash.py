@@ -3,6 +3,9 @@ Algorithm 1: Hash128 from two 64-bit SplitMix64-based hashes, HashCache).
 
 * SplitMix64 against its published outputs from seed 0 (the reference
   implementation's test vector);
+* the hash of a 9-exponent block computed from the definition in Python
+  integers (word packing, key index, length term), with the output function
+  pinned by the same published outputs;
 * the empty block hashes to 0 (fin(0) = 0, a closed form);
 * a change of any single exponent always changes both hashes (each word term
   is a bijection of the word, so the sum moves by a nonzero amount, and the
@@ -24,6 +27,41 @@ def test_splitmix64_published_outputs_from_seed_zero():
     assert oracle.splitmix64(0, 1) == 0xE220A8397B1DCDAF
     assert oracle.splitmix64(0, 2) == 0x6E789E6AA1B965F4
     assert oracle.splitmix64(0, 3) == 0x06C45D188009454F
+
+
+M64 = (1 << 64) - 1
+GOLDEN = 0x9E3779B97F4A7C15
+
+
+def _fin(z):
+    """SplitMix64's output function (Steele, Lea and Flood, 2014), in Python
+    integers; pinned below by the generator's published seed-0 outputs."""
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & M64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & M64
+    return z ^ (z >> 31)
+
+
+def test_nine_exponent_block_hash_from_the_definition():
+    """h_s of a 9-exponent block written out from the definition of the
+    block hash: two little-endian exponent words (the second holds one
+    exponent and seven zero bytes), keys = SplitMix64 outputs 1 and 2 from
+    the seed (state s + i * golden, i = 1, 2), and the length 9 added before
+    the final mix."""
+    # the output function, through the published outputs 1..3 from seed 0
+    assert [_fin(i * GOLDEN & M64) for i in (1, 2, 3)] == [
+        0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+    e = np.array([0x7A, 0x7B, 0x7C, 0x79, 0x80, 0x00, 0xFF, 0x7D, 0x81], np.uint8)
+    word0 = 0x7D_FF_00_80_79_7C_7B_7A      # e0 in the lowest byte
+    word1 = 0x81
+    for seed in (SEED1, SEED2):
+        k1 = _fin((seed + 1 * GOLDEN) & M64)
+        k2 = _fin((seed + 2 * GOLDEN) & M64)
+        h = _fin((9 + _fin(word0 ^ k1) + _fin(word1 ^ k2)) & M64)
+        assert oracle.exp_hash64(e, seed) == h, hex(seed)
+    # and for a block given as bf16 values (exponent = bits 14..7)
+    vals = (e.astype(np.uint16) << 7) | np.uint16(0x8000) | np.uint16(0x0055)
+    assert oracle.block_hash128(vals) == (oracle.exp_hash64(e, SEED1),
+                                          oracle.exp_hash64(e, SEED2))
 
 
 def test_empty_block_hashes_to_zero():

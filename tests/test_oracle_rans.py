@@ -33,6 +33,49 @@ def test_one_symbol_block_by_hand():
     assert st == 0 and out.tolist() == [127]
 
 
+def test_renormalising_block_by_hand():
+    """A 65-exponent block whose lane 0 renormalises twice, derived by hand
+    from the coding step x' = ((x // f) << 12) + x % f + cum[s], preceded by
+    emitting the low 16 bits of x (x >>= 16) whenever x >= f << 20.
+
+    Table: h[127] = 15, h[130] = 1 -> f[127] = 1 + 15*3840/16 = 3601,
+    f[130] = 1 + 3840/16 = 241, the other 254 symbols 1; the sum is 4096, so
+    nothing is added.  cum[127] = 127 (127 symbols of frequency 1 below it);
+    cum[200] = 198 + 3601 + 241 = 4040, cum[201] = 4041, cum[202] = 4042.
+
+    Lane 0 codes positions 0, 32, 64 = symbols 200, 201, 202, backwards:
+      x = 0x10000 (the initial state)
+      s=202: x < 1 << 20;  x = (0x10000 << 12) + 4042        = 0x10000FCA
+      s=201: x >= 1 << 20: emit 0x0FCA, x = 0x1000;
+             x = (0x1000 << 12) + 4041                      = 0x01000FC9
+      s=200: x >= 1 << 20: emit 0x0FC9, x = 0x0100;
+             x = (0x0100 << 12) + 4040                      = 0x00100FC8
+      final state: low 0x0FC8, high 0x0010.
+    Emitted 0x0FCA, 0x0FC9, 0x0FC8, 0x0010; the decoder reads them last
+    first: 0x0010, 0x0FC8, 0x0FC9, 0x0FCA (4 words).
+    Lanes 1..31 code symbol 127 at positions l and l + 32 (f = 3601, bound
+    3601 << 20, never reached):
+      x = 0x10000: 65536 = 18*3601 + 718 -> x = 18*4096 + 718 + 127 = 74573
+      x = 74573 = 20*3601 + 2553 -> x = 20*4096 + 2553 + 127 = 84600 = 0x14A78
+    so each reads 0x0001, 0x4A78 (2 words).
+    Record: 32 uint16 counts (4, then 2 x 31), lane 0's 4 words, 31 x 2
+    words: 64 + 8 + 124 = 196 bytes, zero-padded to 208.
+    """
+    h = np.zeros(256, np.uint32)
+    h[127], h[130] = 15, 1
+    f = oracle.rans_table(h)
+    assert (int(f[127]), int(f[130]), int(f.sum())) == (3601, 241, 4096)
+    e = np.full(65, 127, np.uint8)
+    e[[0, 32, 64]] = [200, 201, 202]
+    words = [4] + [2] * 31 + [0x0010, 0x0FC8, 0x0FC9, 0x0FCA] + [0x0001, 0x4A78] * 31
+    expect = np.array(words, np.uint16).view(np.uint8).tolist() + [0] * 12
+    rec = oracle.rans_encode_block(e, f)
+    assert len(rec) == 208
+    assert rec.tolist() == expect
+    st, out = oracle.rans_decode_block(rec, 65, f)
+    assert st == 0 and out.tolist() == e.tolist()
+
+
 def test_table_normalisation_by_hand():
     h = np.zeros(256, np.uint32)
     h[5], h[9] = 3, 1                 # 1 + 3*3840/4 = 2881, 1 + 3840/4 = 961, 254 x 1
