@@ -8,11 +8,13 @@ exponent caches carried from step to step.  Metric: bf16 weight GB/s =
 2*N bytes per step / time, and the same traffic as a fraction of the
 measured HBM copy bandwidth.
 
-Default workload: one OLMoE-shaped MoE layer (64 experts x {gate, up
-2048x1024, down 1024x2048}, 402,653,184 bf16 values, N(0, 0.02)), 16
-simulated ranks, block 4096, Adam-like step 1e-5 * N(0,1) per iteration.
-Inputs (805 MB per iteration) are larger than the 129 MB L2, so no flush is
-needed between steps.
+Default workload: the fine-grained MoE layer (128 experts x {gate, up
+4096x1536, down 1536x4096}, 2,415,919,104 bf16 values, N(0, 0.015)), 32
+simulated ranks, block 4096, the largest workload that runs as one plan on
+one GPU.  Its iterations step by 2.2e-6, 2.35e-5 and 3.9e-4 times N(0,1)
+(about 0.1 %, 1 % and 10 % of exponents change), five iterations each, so
+the timed steps cover all three rates.  Inputs (4.8 GB per iteration) are
+larger than the 129 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--config 1..5] [--variant clustered0.1]
@@ -50,7 +52,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--config", type=int, default=5)
     ap.add_argument("--variant", default="")
     ap.add_argument("--schedule", choices=["sequential", "pipelined", "graph"],
                     default="sequential",
@@ -64,6 +66,9 @@ def parse_args():
                     help="exact/hash senders: every shard takes the look-back scan, "
                          "even those predicted raw")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=4,
+                    help="end-to-end leg: distinct iterations held in pinned host memory "
+                         "and timed (at most --steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
@@ -178,15 +183,17 @@ def kernel_source_hash(kernel):
     return h.hexdigest()[:16]
 
 
-def traffic_per_value(kernel):
-    """DRAM bytes per value of `kernel` from profiles/traffic.md, or None if
-    that capture was taken on a different kernel source."""
+def traffic_per_value(kernel, workload):
+    """DRAM bytes per value of `kernel` on `workload` (its name without a
+    profiling cut) from profiles/traffic.md, or None if that capture was
+    taken on a different kernel source or no capture covers the workload."""
     try:
         h = kernel_source_hash(kernel)
         for line in open(os.path.join(ROOT, "profiles", "traffic.md")):
             cells = [c.strip() for c in line.strip().strip("|").split("|")]
-            if len(cells) >= 3 and cells[0] == kernel and cells[1] == h:
-                return float(cells[2])
+            if (len(cells) >= 4 and cells[0] == kernel and cells[1] == h
+                    and cells[2] == workload):
+                return float(cells[3])
     except (OSError, ValueError):
         pass
     return None
@@ -251,14 +258,6 @@ def algorithmic_bytes(descs, numel, hashed=False, block=4096):
         changed = sum(d["n_changed_blocks"] for d in descs)
         return 2 * numel + 16 * blocks + P + 16 * changed, 3 * numel + P, C / max(numel, 1)
     return 3 * numel + P + C, 3 * numel + P, C / max(numel, 1)
-
-
-def gen_sequence(wl, iterations, device, layer=0):
-    from lossless_exponent_reuse_gb300 import workloads
-    seq = [workloads.initial_layer(wl, layer, device)]
-    for t in range(1, iterations):
-        seq.append(workloads.step_layer(wl, seq[-1], layer, t))
-    return seq
 
 
 def accepted_tensors(wl):
@@ -453,12 +452,13 @@ def run_ours(args, world, rank, local):
         bytes_d.append(bd)
         fvals.append(fsum / L)
         wire.append(pw / (n * L))
-    # exponent change rate between consecutive timed iterations (first layer)
+    # exponent change rate between consecutive timed iterations (first layer):
+    # the exponent is bits 14..7, so it changed where those bits differ
     exp_rates = []
     for i in range(1, K):
-        e0 = (seq[i - 1][0].view(torch.int16).to(torch.int32) >> 7) & 0xFF
-        e1 = (seq[i][0].view(torch.int16).to(torch.int32) >> 7) & 0xFF
-        exp_rates.append(float((e0 != e1).float().mean()))
+        diff = (seq[i - 1][0].view(torch.int16) ^ seq[i][0].view(torch.int16)) & 0x7F80
+        exp_rates.append(float(torch.count_nonzero(diff)) / max(n, 1))
+        del diff
     torch.cuda.synchronize()
     # the receiver's critical path alone (the paper's Decmp): every layer's
     # gather-decompress again on the final payloads (it is idempotent there)
@@ -506,10 +506,16 @@ def run_ours(args, world, rank, local):
         dom = kname
     elif rans and t_c is not None:
         dom += "+k_decompress_rans"
+    base_name = workloads.workload(args.config).name
     tpv = (traffic_per_value(kname if dom == kname else
-                             ("k_decompress_rans" if rans else "k_decompress"))
+                             ("k_decompress_rans" if rans else "k_decompress"),
+                             base_name + (f"_{args.variant}" if args.variant else ""))
            if t_c is not None else None)
     traffic = round(tpv * n) if tpv is not None else None
+    # the same kernel against the copy bandwidth in the DRAM bytes ncu counted
+    # (algorithmic bytes count every changed value's cache refresh, which the
+    # kernel writes only for the 16-byte groups that differ)
+    dram_gbs = traffic / (dom_ms / 1e3) / 1e9 if traffic is not None else None
     cfg = {"workload": wl.name, "sender": args.sender, "schedule": sched, "numel": n * L,
            "layers": L,
            "numel_per_plan": n,
@@ -539,7 +545,9 @@ def run_ours(args, world, rank, local):
         "decompress_only_ms": round(decompress_only_ms, 4),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "peak_kind": peak_kind},
+                     "traffic": traffic, "peak_kind": peak_kind,
+                     "achieved_dram": round(dram_gbs, 1) if dram_gbs is not None else None,
+                     "frac_dram": round(dram_gbs / peak, 4) if dram_gbs is not None else None},
         # exact/hashed: compress, repack (raw-ahead plans), bitmap scan,
         # decompress; RANS: coder tables, compress, raw fixup, bitmap scan,
         # slot tables, decompress
@@ -565,78 +573,89 @@ def run_ours(args, world, rank, local):
     del layers
     torch.cuda.empty_cache()
     if not args.no_e2e:
-        if L == 1:
-            result["e2e"] = run_e2e(wl, [s_[0] for s_ in seq], n, K, dev, world, hashed, rans,
-                                    raw_ahead)
+        if L == 1 and not (hashed or rans):
+            steps = max(1, min(K, args.e2e_steps))
+            inputs = [s_[0] for s_ in seq[:steps]]
+            del seq
+            result["e2e"] = run_e2e(wl, inputs, n, dev, world, raw_ahead)
+            del inputs
         else:
             result["e2e"] = None
-    del seq
+    else:
+        del seq
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, warm_host, 1, args.cpu_seconds)
     return result
 
 
-def run_e2e(wl, seq, n, K, dev, world, hashed=False, rans=False, raw_ahead=True):
-    """The same metric through host buffers: each step copies its weights
-    from pinned host memory, runs the path and copies the rebuilt weights
-    back, with neighbouring steps' uploads and downloads overlapped
-    (HostStreamer).  A fresh state is warmed up on the first three inputs
-    (the first call is the cold start); then all K inputs are timed in order."""
+def run_e2e(wl, seq, n, dev, world, raw_ahead=True):
+    """The same metric through the C ABI with host buffers: each step is one
+    ciera_step_host call, which copies that step's weights from pinned host
+    memory, runs the sender and the gather-decompress, and copies the rebuilt
+    weights back, in chunks of ranks whose copies overlap the kernels.  A
+    fresh state is warmed up on the inputs first (the first call is the cold
+    start); then every input is timed once, in order."""
     from lossless_exponent_reuse_gb300 import ciera
-    from lossless_exponent_reuse_gb300.allgather import HostStreamer, SimulatedAllgather
+    from lossless_exponent_reuse_gb300.allgather import SimulatedAllgather
+    K = len(seq)
     host = [s.view(torch.int16).to("cpu").pin_memory() for s in seq]
-    outs = [torch.empty(n, dtype=torch.int16).pin_memory() for _ in range(2)]
-    ag = SimulatedAllgather(n, wl.block, wl.ranks, device=dev, hashed=hashed, rans=rans,
-                            raw_ahead=raw_ahead)
-    hs = HostStreamer(ag)
+    del seq
+    torch.cuda.empty_cache()
+    out_host = torch.empty(n, dtype=torch.int16).pin_memory()
+    w_dev = torch.empty(n, dtype=torch.int16, device=dev)
+    chunks = min(wl.ranks, 16)
+    ag = SimulatedAllgather(n, wl.block, wl.ranks, device=dev, raw_ahead=raw_ahead)
+    session = ciera.HostSession(chunks)
     stream = torch.cuda.current_stream()
-    for t in range(min(3, len(host))):               # warm-up (first call is the cold start)
-        hs.step(host[t], outs[t % 2])
-    hs.finish()
+    for t in range(min(3, K)):                        # warm-up (first call is the cold start)
+        ag.step_host(session, host[t], out_host, w_dev, chunks=chunks)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     start.record(stream)
     for i in range(K):
-        hs.step(host[i], outs[i % 2])
-    hs.finish()
+        ag.step_host(session, host[i], out_host, w_dev, chunks=chunks)
     end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     if ag.status() != ciera.OK:
         raise RuntimeError("e2e steps reported an error status")
-    if not torch.equal(outs[(K - 1) % 2], host[K - 1].view(torch.int16)):
+    if not torch.equal(out_host, host[K - 1]):
         raise RuntimeError("e2e round trip is not exact")
     t = max_over_ranks(world, start.elapsed_time(end) / 1e3)
     val = 2.0 * sum_over_ranks(world, float(n * K)) / t / 1e9
-    link = link_bound(host, outs, hs, K, stream)
+    del ag
+    link = link_bound(host, out_host, w_dev, stream)
     return {"value": round(val, 2), "unit": UNIT, "h2d_bytes_per_step": 2 * n,
-            "d2h_bytes_per_step": 2 * n,
+            "d2h_bytes_per_step": 2 * n, "steps": K, "chunks": chunks,
+            "api": "ciera_step_host (C ABI, pinned host buffers)",
             # the same bytes moved by plain copies alone, both directions at
-            # once on the same streams: what this box's host link allows
-            "link_bound": round(link, 2)}
+            # once on two streams: what this box's host link allows
+            "link_bound": round(link, 2), "frac_of_link": round(val / link, 4)}
 
 
-def link_bound(host, outs, hs, K, stream):
+def link_bound(host, out_host, w_dev, stream):
     """bf16 GB/s that the host link alone sustains for the e2e traffic: each
-    of K steps uploads one input (pinned) and downloads one output of the same
-    size, on the HostStreamer's two copy streams at the same time, with no
-    kernel in between.  The e2e figure divided by this is the share of the
-    link the path uses; boxes differ in this bound, the kernels do not."""
-    dev_in, dev_out = hs.w_buf, hs.out_buf
+    step uploads one input (pinned) and downloads one output of the same size,
+    on two streams at the same time, with no kernel.  The e2e figure divided
+    by this is the share of the link the path uses; boxes differ in this
+    bound, the kernels do not."""
     n = host[0].numel()
+    K = len(host)
+    src = torch.empty(n, dtype=torch.int16, device=w_dev.device)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     start.record(stream)
-    hs.s_in.wait_stream(stream)
-    hs.s_out.wait_stream(stream)
+    s_in.wait_stream(stream)
+    s_out.wait_stream(stream)
     for i in range(K):
-        with torch.cuda.stream(hs.s_in):
-            dev_in[i % 2][:n].copy_(host[i].view(torch.int16), non_blocking=True)
-        with torch.cuda.stream(hs.s_out):
-            outs[i % 2].copy_(dev_out[i % 2][:n], non_blocking=True)
-    stream.wait_stream(hs.s_in)
-    stream.wait_stream(hs.s_out)
+        with torch.cuda.stream(s_in):
+            w_dev[:n].copy_(host[i], non_blocking=True)
+        with torch.cuda.stream(s_out):
+            out_host.copy_(src, non_blocking=True)
+    stream.wait_stream(s_in)
+    stream.wait_stream(s_out)
     end.record(stream)
     torch.cuda.synchronize()
     return 2.0 * n * K / (start.elapsed_time(end) / 1e3) / 1e9
@@ -653,8 +672,17 @@ def run_reference(args, world, rank):
     W, K = args.warmup, args.steps
     # each step: one rank's shard of one iteration, compress + decompress
     S = oracle.shard_size(n, R)
-    seq = gen_sequence(wl, W + K + 1, "cpu")
-    seq_host = [s.numpy() for s in seq]
+    # input generation only (not timed): on the GPU when there is one, since
+    # a 2.4 G-value layer draws slowly on the host; rank 0's shard is kept
+    gdev = "cuda" if torch.cuda.is_available() else "cpu"
+    from lossless_exponent_reuse_gb300 import workloads as _wl
+    seq_host = []
+    w = _wl.initial_layer(wl, 0, gdev)
+    for t in range(W + K + 1):
+        if t > 0:
+            w = _wl.step_layer(wl, w, 0, t)
+        seq_host.append(w[:S].view(torch.int16).cpu().numpy().view(np.uint16).copy())
+    del w
     threads = 1
     sc = np.zeros(S, np.uint8)
     rc = np.zeros(S, np.uint8)

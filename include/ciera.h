@@ -252,6 +252,61 @@ int ciera_decompress(ciera_plan_t plan, const uint8_t *payloads_dev, int64_t pay
                      const ciera_desc *descs_dev, uint8_t *recv_cache_dev, uint16_t *out_dev,
                      void *workspace_dev, uint32_t flags, void *stream);
 
+/* Receiver side with the R payloads in separate buffers, as a grouped
+ * broadcast or any other collective that lands each rank's payload in its
+ * own buffer would deliver them (Algorithm 1, receiver: one Recv() per
+ * shard).  Same work and results as ciera_decompress.
+ *   payload_ptrs_dev  device memory: an array of R device pointers, rank r's
+ *                     payload at payload_ptrs_dev[r]; the array 8-byte aligned
+ *   payload_capacity  bytes each of those buffers holds, at least
+ *                     info.payload_capacity
+ * Other arguments as ciera_decompress.  The pointers are read by the
+ * kernels: a rank whose pointer is NULL, or (on the fast path) not 16-byte
+ * aligned, is skipped like a corrupt payload and CIERA_E_CORRUPT recorded.
+ * Errors: CIERA_E_INVAL (as ciera_decompress, a NULL or misaligned table, a
+ * short capacity), CIERA_E_CUDA. */
+int ciera_decompress_gather(ciera_plan_t plan, const uint8_t *const *payload_ptrs_dev,
+                            int64_t payload_capacity, const ciera_desc *descs_dev,
+                            uint8_t *recv_cache_dev, uint16_t *out_dev, void *workspace_dev,
+                            uint32_t flags, void *stream);
+
+/* One step from host memory and back: the sender side for all ranks and the
+ * gather-decompress, with the weights read from host memory and the rebuilt
+ * weights written to host memory (Algorithm 1 from Send to the merged
+ * output), in one call.  A session owns the two copy streams and the events
+ * that order them; it must not be used by two calls at once.
+ *   max_chunks  the largest `chunks` a step of this session may use
+ * Errors: CIERA_E_INVAL (max_chunks < 1, NULL out), CIERA_E_CUDA. */
+typedef struct ciera_host_session_s *ciera_host_session_t;
+int ciera_host_session_create(int max_chunks, ciera_host_session_t *out);
+void ciera_host_session_destroy(ciera_host_session_t session);
+
+/* The ranks are cut into `chunks` consecutive groups of ceil(R/chunks)
+ * ranks.  For each group, in order: its values are copied from w_host into
+ * w_dev on the session's upload stream; `stream` runs ciera_compress and
+ * the receiver for those ranks once they have arrived; the session's
+ * download stream copies the group's rebuilt values from out_dev to
+ * out_host.  So the upload of one group, the kernels of the one before and
+ * the download of the one before that overlap.  The step begins after the
+ * work already queued on `stream` and everything it does, copies included,
+ * is ordered before later work on `stream`: out_host holds the rebuilt
+ * values once `stream` has been synchronised.
+ *   w_host, out_host   N bf16 values in host memory; pinned (page-locked)
+ *                      for the copies to run asynchronously and overlap
+ *   w_dev, out_dev     N-value device buffers the call copies into / from
+ *   the rest           as ciera_compress (all ranks: sender_cache_dev,
+ *                      payloads_dev, payload_stride, descs_dev, flags) and
+ *                      ciera_decompress (recv_cache_dev); one workspace
+ *                      serves both, and ciera_status() reads its status
+ *   chunks             1 .. the session's max_chunks (more than R acts as R)
+ * Results equal those of ciera_compress and ciera_decompress over all ranks.
+ * Errors: CIERA_E_INVAL, CIERA_E_CUDA. */
+int ciera_step_host(ciera_host_session_t session, ciera_plan_t plan, const uint16_t *w_host,
+                    uint16_t *out_host, uint16_t *w_dev, uint8_t *sender_cache_dev,
+                    uint8_t *payloads_dev, int64_t payload_stride, ciera_desc *descs_dev,
+                    uint8_t *recv_cache_dev, uint16_t *out_dev, void *workspace_dev,
+                    uint32_t flags, int chunks, void *stream);
+
 /* Wait for `stream`, then read and clear the workspace's status word.
  * Returns CIERA_OK, CIERA_E_CORRUPT, CIERA_E_TIMEOUT, CIERA_E_INTERNAL,
  * CIERA_E_BOUNDS (checked builds only) or CIERA_E_CUDA. */

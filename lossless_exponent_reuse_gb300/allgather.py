@@ -79,66 +79,23 @@ class SimulatedAllgather:
         self.compress(w, stream=stream)
         return self.decompress(stream=stream)
 
-    def step_host(self, w_host: torch.Tensor, out_host: torch.Tensor, w_dev: torch.Tensor,
+    def step_host(self, session: ciera.HostSession, w_host: torch.Tensor,
+                  out_host: torch.Tensor, w_dev: torch.Tensor, chunks: int = 1,
                   stream=None) -> None:
-        """End-to-end from host memory: copy this iteration's weights in,
-        run the path, copy the rebuilt weights out (pinned buffers)."""
-        w_dev.view(torch.int16).copy_(w_host.view(torch.int16), non_blocking=True)
-        self.step(w_dev, stream=stream)
-        out_host.view(torch.int16).copy_(self.out[: self.numel].view(torch.int16),
-                                         non_blocking=True)
+        """End-to-end from host memory (ciera_step_host): this iteration's
+        weights are copied in from ``w_host`` (pinned) to ``w_dev``, the path
+        runs, and the rebuilt weights land in ``out_host``, in chunks of ranks
+        whose copies overlap the kernels.  Exact sender only."""
+        if self.rans or self.hashed:
+            raise ValueError("step_host drives the exact sender")
+        session.step(self.plan, w_host, out_host, w_dev, self.sender_cache, self.payloads,
+                     self.descs, self.recv_cache, self.out, self.workspace,
+                     cold=self.iteration == 0, extra_flags=self.extra_flags, chunks=chunks,
+                     stream=stream)
+        self.iteration += 1
 
     def status(self, stream=None) -> int:
         return ciera.status(self.workspace, stream=stream)
 
     def descriptors(self):
         return ciera.decode_descs(self.descs)
-
-
-class HostStreamer:
-    """Steps whose weights come from pinned host memory and whose rebuilt
-    weights go back to it, with the copies of neighbouring steps overlapped:
-    the upload of step i+1 and the download of step i run on their own
-    streams (the link carries both directions at once) while the path runs on
-    the caller's stream.  Device staging is double-buffered and every reuse
-    of a buffer waits, by event, for its previous reader."""
-
-    def __init__(self, ag: SimulatedAllgather):
-        n = max(ag.numel, 1)
-        dev = ag.device
-        self.ag = ag
-        self.w_buf = [torch.empty(n, dtype=torch.int16, device=dev) for _ in range(2)]
-        self.out_buf = [torch.empty(n, dtype=torch.int16, device=dev) for _ in range(2)]
-        self.s_in = torch.cuda.Stream(device=dev)
-        self.s_out = torch.cuda.Stream(device=dev)
-        ev = lambda: [torch.cuda.Event() for _ in range(2)]
-        self.ev_in, self.ev_done, self.ev_out = ev(), ev(), ev()
-        self.count = 0
-
-    def step(self, w_host: torch.Tensor, out_host: torch.Tensor) -> None:
-        """Enqueue one step (asynchronous; ``finish`` joins it)."""
-        n = self.ag.numel
-        b = self.count % 2
-        compute = torch.cuda.current_stream(self.ag.device)
-        if self.count >= 2:
-            self.s_in.wait_event(self.ev_done[b])        # step count-2 has read w_buf[b]
-        with torch.cuda.stream(self.s_in):
-            self.w_buf[b][:n].copy_(w_host.view(torch.int16), non_blocking=True)
-            self.ev_in[b].record(self.s_in)
-        compute.wait_event(self.ev_in[b])
-        if self.count >= 2:
-            compute.wait_event(self.ev_out[b])           # step count-2 has left out_buf[b]
-        self.ag.compress(self.w_buf[b][:n])
-        self.ag.decompress(out=self.out_buf[b])
-        self.ev_done[b].record(compute)
-        self.s_out.wait_event(self.ev_done[b])
-        with torch.cuda.stream(self.s_out):
-            out_host.view(torch.int16).copy_(self.out_buf[b][:n], non_blocking=True)
-            self.ev_out[b].record(self.s_out)
-        self.count += 1
-
-    def finish(self) -> None:
-        """Make the caller's stream wait for every enqueued copy."""
-        compute = torch.cuda.current_stream(self.ag.device)
-        compute.wait_stream(self.s_in)
-        compute.wait_stream(self.s_out)

@@ -89,6 +89,11 @@ SIGNATURES = {
                                    _u32, _vp]),
     "ciera_compress_noalloc": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _u32,
                                       _vp]),
+    "ciera_decompress_gather": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _u32, _vp]),
+    "ciera_host_session_create": (_i32, [_i32, ctypes.POINTER(_vp)]),
+    "ciera_host_session_destroy": (None, [_vp]),
+    "ciera_step_host": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp,
+                               _u32, _i32, _vp]),
     "ciera_pipeline_create": (_i32, [_i32, ctypes.POINTER(_vp)]),
     "ciera_pipeline_destroy": (None, [_vp]),
     "ciera_pipeline_step": (_i32, [_vp, _vp, _i32, _vp, _vp]),
@@ -321,6 +326,69 @@ class Plan:
             _dev_ptr(workspace, "workspace", torch.uint8), DECOMPRESS_RANS if rans else 0,
             _stream_handle(stream)),
             "ciera_decompress")
+
+
+    def decompress_gather(self, payload_ptrs: torch.Tensor, payload_capacity: int,
+                          descs: torch.Tensor, recv_cache: torch.Tensor, out: torch.Tensor,
+                          workspace: torch.Tensor, *, rans: bool = False, stream=None) -> None:
+        """ciera_decompress_gather: ``payload_ptrs`` is a device int64 tensor of
+        R device addresses (each buffer ``payload_capacity`` bytes or more)."""
+        info = self.info
+        if payload_ptrs.dtype != torch.int64 or payload_ptrs.numel() < info.ranks:
+            raise ValueError("payload_ptrs must hold R int64 device addresses")
+        if descs.numel() < info.ranks * DESC_BYTES:
+            raise ValueError("descs too small")
+        if workspace.numel() < info.workspace_bytes:
+            raise ValueError("workspace too small")
+        _check(lib().ciera_decompress_gather(
+            self._h, _dev_ptr(payload_ptrs, "payload_ptrs"), int(payload_capacity),
+            _dev_ptr(descs, "descs", torch.uint8),
+            _dev_ptr(recv_cache, "recv_cache", torch.uint8, info.numel),
+            _dev_ptr(out, "out", torch.uint16, info.numel),
+            _dev_ptr(workspace, "workspace", torch.uint8), DECOMPRESS_RANS if rans else 0,
+            _stream_handle(stream)),
+            "ciera_decompress_gather")
+
+
+class HostSession:
+    """ciera_host_session_* and ciera_step_host: steps whose weights come
+    from host memory and whose rebuilt weights go back to it, in one call."""
+
+    def __init__(self, max_chunks: int):
+        h = ctypes.c_void_p()
+        _check(lib().ciera_host_session_create(int(max_chunks), ctypes.byref(h)),
+               "ciera_host_session_create")
+        self._h = h
+        self.max_chunks = max_chunks
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and _lib is not None:
+            _lib.ciera_host_session_destroy(h)
+            self._h = None
+
+    def step(self, plan: Plan, w_host: torch.Tensor, out_host: torch.Tensor,
+             w_dev: torch.Tensor, sender_cache: torch.Tensor, payloads: torch.Tensor,
+             descs: torch.Tensor, recv_cache: torch.Tensor, out_dev: torch.Tensor,
+             workspace: torch.Tensor, *, cold: bool = False, extra_flags: int = 0,
+             chunks: int = 1, stream=None) -> None:
+        n = plan.info.numel
+        for name, t in (("w_host", w_host), ("out_host", out_host)):
+            if t.is_cuda or not t.is_contiguous() or t.numel() < n or t.element_size() != 2:
+                raise ValueError(f"{name} must be a contiguous 16-bit host tensor of N values")
+        if payloads.dim() != 2 or payloads.shape[0] < plan.info.ranks:
+            raise ValueError("payloads must be [ranks, stride] uint8")
+        _check(lib().ciera_step_host(
+            self._h, plan.handle, w_host.data_ptr() if n else None,
+            out_host.data_ptr() if n else None, _dev_ptr(w_dev, "w_dev", torch.uint16, n),
+            _dev_ptr(sender_cache, "sender_cache", torch.uint8, n),
+            _dev_ptr(payloads, "payloads", torch.uint8), payloads.stride(0),
+            _dev_ptr(descs, "descs", torch.uint8),
+            _dev_ptr(recv_cache, "recv_cache", torch.uint8, n),
+            _dev_ptr(out_dev, "out_dev", torch.uint16, n),
+            _dev_ptr(workspace, "workspace", torch.uint8),
+            (COLD if cold else 0) | int(extra_flags), int(chunks), _stream_handle(stream)),
+            "ciera_step_host")
 
 
 def status(workspace: torch.Tensor, stream=None) -> int:

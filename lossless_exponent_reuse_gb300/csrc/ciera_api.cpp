@@ -313,6 +313,62 @@ int ciera_compress_rans(ciera_plan_t p, int rank_begin, int rank_count, const ui
 
 }  // extern "C"
 
+namespace {
+
+// Receiver for ranks [rb, rb + rc) (Section 3.1; Algorithm 1, receiver).
+// Every array is plan-wide and indexed by absolute rank or value: the
+// payloads contiguous (rank r at payloads_dev + r*stride) or given by a
+// device table of R pointers (each buffer holding at least `stride` bytes),
+// the R descriptors, the N-value ExpCache and output; the workspace regions
+// are per absolute rank too, so ranges of one plan may share a workspace.
+int decompress_impl(ciera_plan_t p, int rb, int rc, const uint8_t* payloads_dev,
+                    const uint8_t* const* payload_ptrs_dev, int64_t stride,
+                    const ciera_desc* descs_dev, uint8_t* recv_cache_dev, uint16_t* out_dev,
+                    void* workspace_dev, uint32_t flags, void* stream) {
+  if (!p || rb < 0 || rc < 1 || static_cast<int64_t>(rb) + rc > p->ranks || !descs_dev ||
+      !workspace_dev || (flags & ~CIERA_DECOMPRESS_RANS))
+    return CIERA_E_INVAL;
+  if (p->numel > 0 && (!recv_cache_dev || !out_dev)) return CIERA_E_INVAL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace_dev);
+  const int64_t first = static_cast<int64_t>(rb) * p->S;  // first value of the range
+  DecompressParams kp{};
+  kp.geo = range_geometry(p, rb, rc);
+  kp.payloads = payloads_dev ? payloads_dev + rb * stride : nullptr;
+  kp.payload_ptrs = payload_ptrs_dev ? payload_ptrs_dev + rb : nullptr;
+  kp.stride = stride;
+  kp.descs = descs_dev + rb;
+  kp.rcache = recv_cache_dev ? recv_cache_dev + first : nullptr;
+  kp.out = out_dev ? out_dev + first : nullptr;
+  kp.bm_words = reinterpret_cast<uint32_t*>(ws + p->off_words) + rb * p->nw_stride;
+  kp.bm_prefix = reinterpret_cast<uint32_t*>(ws + p->off_prefix) + rb * p->nw_stride;
+  kp.nw_stride = p->nw_stride;
+  kp.rank_state = reinterpret_cast<uint32_t*>(ws + p->off_rstate) + rb;
+  kp.ctl = reinterpret_cast<Control*>(ws);
+  kp.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  // with a pointer table, each payload's alignment is checked by the bitmap
+  // scan (a misaligned one is reported corrupt)
+  kp.fast = p->fast && (payload_ptrs_dev || (aligned16(payloads_dev) && stride % 16 == 0)) &&
+            aligned16(kp.rcache) && aligned16(kp.out);
+  int e;
+  if (flags & CIERA_DECOMPRESS_RANS) {
+    if (!kp.fast || p->numel % 16 != 0) return CIERA_E_INVAL;
+    kp.rans = 1;
+    // the bitmap scan alone (no tiles), then the RANS receiver, which takes
+    // the RAW ranks too
+    DecompressParams scan = kp;
+    scan.geo.total_tiles = 0;
+    e = launch_decompress(scan, 0, stream);
+    if (e == cudaSuccess)
+      e = launch_decompress_rans(
+          kp, reinterpret_cast<uint32_t*>(ws + p->off_rdec + kRansDecTableBytes * rb), stream);
+  } else {
+    e = launch_decompress(kp, kp.fast ? p->smem_decompress : 0, stream);
+  }
+  return e == cudaSuccess ? CIERA_OK : CIERA_E_CUDA;
+}
+
+}  // namespace
+
 struct ciera_pipeline_s {
   int max_layers;
   cudaEvent_t fork;
@@ -391,41 +447,21 @@ int ciera_pipeline_step(ciera_pipeline_t pp, const ciera_layer* layers, int n, v
 int ciera_decompress(ciera_plan_t p, const uint8_t* payloads_dev, int64_t payload_stride,
                      const ciera_desc* descs_dev, uint8_t* recv_cache_dev, uint16_t* out_dev,
                      void* workspace_dev, uint32_t flags, void* stream) {
-  if (!p || !payloads_dev || !descs_dev || !workspace_dev || payload_stride < p->capacity ||
-      (flags & ~CIERA_DECOMPRESS_RANS))
+  if (!p || !payloads_dev || payload_stride < p->capacity) return CIERA_E_INVAL;
+  return decompress_impl(p, 0, static_cast<int>(p->ranks), payloads_dev, nullptr, payload_stride,
+                         descs_dev, recv_cache_dev, out_dev, workspace_dev, flags, stream);
+}
+
+int ciera_decompress_gather(ciera_plan_t p, const uint8_t* const* payload_ptrs_dev,
+                            int64_t payload_capacity, const ciera_desc* descs_dev,
+                            uint8_t* recv_cache_dev, uint16_t* out_dev, void* workspace_dev,
+                            uint32_t flags, void* stream) {
+  if (!p || !payload_ptrs_dev || payload_capacity < p->capacity ||
+      (reinterpret_cast<uintptr_t>(payload_ptrs_dev) & 7u))
     return CIERA_E_INVAL;
-  if (p->numel > 0 && (!recv_cache_dev || !out_dev)) return CIERA_E_INVAL;
-  uint8_t* ws = static_cast<uint8_t*>(workspace_dev);
-  DecompressParams kp{};
-  kp.geo = range_geometry(p, 0, p->ranks);
-  kp.payloads = payloads_dev;
-  kp.stride = payload_stride;
-  kp.descs = descs_dev;
-  kp.rcache = recv_cache_dev;
-  kp.out = out_dev;
-  kp.bm_words = reinterpret_cast<uint32_t*>(ws + p->off_words);
-  kp.bm_prefix = reinterpret_cast<uint32_t*>(ws + p->off_prefix);
-  kp.nw_stride = p->nw_stride;
-  kp.rank_state = reinterpret_cast<uint32_t*>(ws + p->off_rstate);
-  kp.ctl = reinterpret_cast<Control*>(ws);
-  kp.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
-  kp.fast = p->fast && aligned16(payloads_dev) && (payload_stride % 16 == 0) &&
-            aligned16(recv_cache_dev) && aligned16(out_dev);
-  int e;
-  if (flags & CIERA_DECOMPRESS_RANS) {
-    if (!kp.fast || p->numel % 16 != 0) return CIERA_E_INVAL;
-    kp.rans = 1;
-    // the bitmap scan alone (no tiles), then the RANS receiver, which takes
-    // the RAW ranks too
-    DecompressParams scan = kp;
-    scan.geo.total_tiles = 0;
-    e = launch_decompress(scan, 0, stream);
-    if (e == cudaSuccess)
-      e = launch_decompress_rans(kp, reinterpret_cast<uint32_t*>(ws + p->off_rdec), stream);
-  } else {
-    e = launch_decompress(kp, kp.fast ? p->smem_decompress : 0, stream);
-  }
-  return e == cudaSuccess ? CIERA_OK : CIERA_E_CUDA;
+  return decompress_impl(p, 0, static_cast<int>(p->ranks), nullptr, payload_ptrs_dev,
+                         payload_capacity, descs_dev, recv_cache_dev, out_dev, workspace_dev,
+                         flags, stream);
 }
 
 int ciera_status(void* workspace_dev, void* stream) {
@@ -530,6 +566,112 @@ int ciera_get_cost_model(ciera_cost_model* model) {
 int ciera_set_wait_timeout_ns(uint64_t ns) {
   if (ns == 0) return CIERA_E_INVAL;
   g_timeout_ns.store(ns, std::memory_order_relaxed);
+  return CIERA_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// One step from host memory and back (Algorithm 1's Send / Recv boundary as a
+// single call): upload, sender, receiver and download, in chunks of ranks so
+// that the upload of chunk c+1, the kernels of chunk c and the download of
+// chunk c-1 run at the same time.
+
+struct ciera_host_session_s {
+  int max_chunks = 0;
+  cudaStream_t s_in = nullptr, s_out = nullptr;  // upload and download streams
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::vector<cudaEvent_t> uploaded, rebuilt;    // per chunk
+};
+
+extern "C" {
+
+void ciera_host_session_destroy(ciera_host_session_t h) {
+  if (!h) return;
+  for (cudaEvent_t e : h->uploaded)
+    if (e) cudaEventDestroy(e);
+  for (cudaEvent_t e : h->rebuilt)
+    if (e) cudaEventDestroy(e);
+  if (h->fork) cudaEventDestroy(h->fork);
+  if (h->join) cudaEventDestroy(h->join);
+  if (h->s_in) cudaStreamDestroy(h->s_in);
+  if (h->s_out) cudaStreamDestroy(h->s_out);
+  delete h;
+}
+
+int ciera_host_session_create(int max_chunks, ciera_host_session_t* out) {
+  if (!out || max_chunks < 1) return CIERA_E_INVAL;
+  ciera_host_session_s* h = new (std::nothrow) ciera_host_session_s();
+  if (!h) return CIERA_E_INVAL;
+  h->max_chunks = max_chunks;
+  h->uploaded.assign(static_cast<size_t>(max_chunks), nullptr);
+  h->rebuilt.assign(static_cast<size_t>(max_chunks), nullptr);
+  bool ok = cudaStreamCreateWithFlags(&h->s_in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h->fork, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h->join, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; ok && i < max_chunks; ++i)
+    ok = cudaEventCreateWithFlags(&h->uploaded[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&h->rebuilt[i], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    ciera_host_session_destroy(h);
+    return CIERA_E_CUDA;
+  }
+  *out = h;
+  return CIERA_OK;
+}
+
+int ciera_step_host(ciera_host_session_t h, ciera_plan_t p, const uint16_t* w_host,
+                    uint16_t* out_host, uint16_t* w_dev, uint8_t* sender_cache_dev,
+                    uint8_t* payloads_dev, int64_t payload_stride, ciera_desc* descs_dev,
+                    uint8_t* recv_cache_dev, uint16_t* out_dev, void* workspace_dev,
+                    uint32_t flags, int chunks, void* stream) {
+  if (!h || !p || chunks < 1 || chunks > h->max_chunks || (flags & ~kCompressFlags))
+    return CIERA_E_INVAL;
+  if (p->numel > 0 && (!w_host || !out_host || !w_dev || !out_dev)) return CIERA_E_INVAL;
+  if (!payloads_dev || !descs_dev || !workspace_dev || payload_stride < p->capacity)
+    return CIERA_E_INVAL;
+  const int64_t R = p->ranks;
+  const int64_t per = ceil_div(R, chunks < R ? chunks : R);  // ranks per chunk
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // fork: the copy streams start after what is already queued on `stream`
+  if (cudaEventRecord(h->fork, s) != cudaSuccess ||
+      cudaStreamWaitEvent(h->s_in, h->fork, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(h->s_out, h->fork, 0) != cudaSuccess)
+    return CIERA_E_CUDA;
+  int c = 0;
+  for (int64_t rb = 0; rb < R; rb += per, ++c) {
+    const int64_t rc = rb + per < R ? per : R - rb;
+    const int64_t v0 = rb * p->S < p->numel ? rb * p->S : p->numel;
+    const int64_t v1 = (rb + rc) * p->S < p->numel ? (rb + rc) * p->S : p->numel;
+    const size_t bytes = static_cast<size_t>(2 * (v1 - v0));
+    if (bytes > 0 && cudaMemcpyAsync(w_dev + v0, w_host + v0, bytes, cudaMemcpyHostToDevice,
+                                     h->s_in) != cudaSuccess)
+      return CIERA_E_CUDA;
+    if (cudaEventRecord(h->uploaded[c], h->s_in) != cudaSuccess ||
+        cudaStreamWaitEvent(s, h->uploaded[c], 0) != cudaSuccess)
+      return CIERA_E_CUDA;
+    int rcode = ciera_compress(p, static_cast<int>(rb), static_cast<int>(rc), w_dev + v0,
+                               sender_cache_dev ? sender_cache_dev + v0 : nullptr,
+                               payloads_dev ? payloads_dev + rb * payload_stride : nullptr,
+                               payload_stride, descs_dev ? descs_dev + rb : nullptr, nullptr,
+                               workspace_dev, flags, s);
+    if (rcode != CIERA_OK) return rcode;
+    rcode = decompress_impl(p, static_cast<int>(rb), static_cast<int>(rc), payloads_dev, nullptr,
+                            payload_stride, descs_dev, recv_cache_dev, out_dev, workspace_dev, 0,
+                            s);
+    if (rcode != CIERA_OK) return rcode;
+    if (cudaEventRecord(h->rebuilt[c], s) != cudaSuccess ||
+        cudaStreamWaitEvent(h->s_out, h->rebuilt[c], 0) != cudaSuccess)
+      return CIERA_E_CUDA;
+    if (bytes > 0 && cudaMemcpyAsync(out_host + v0, out_dev + v0, bytes, cudaMemcpyDeviceToHost,
+                                     h->s_out) != cudaSuccess)
+      return CIERA_E_CUDA;
+  }
+  // join: every upload precedes a kernel on `stream`; wait for the downloads
+  if (cudaEventRecord(h->join, h->s_out) != cudaSuccess ||
+      cudaStreamWaitEvent(s, h->join, 0) != cudaSuccess)
+    return CIERA_E_CUDA;
   return CIERA_OK;
 }
 

@@ -155,6 +155,13 @@ __device__ __forceinline__ bool in_bounds(Control* ctl, int64_t off, int64_t siz
   return false;
 }
 
+// Received payload of range rank r: its entry of the pointer table when the
+// payloads arrived in separate buffers, else its slot of the contiguous
+// layout.  p.stride bounds either.
+__device__ __forceinline__ const uint8_t* payload_of(const DecompressParams& p, int64_t r) {
+  return p.payload_ptrs ? p.payload_ptrs[r] : p.payloads + r * p.stride;
+}
+
 // Named barrier of the 96 worker threads (warps 1-3) of a compress CTA.
 __device__ __forceinline__ void flaggers_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 32) : "memory");

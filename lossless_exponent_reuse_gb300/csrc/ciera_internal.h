@@ -114,9 +114,10 @@ struct CompressParams {
 };
 
 struct DecompressParams {
-  Geometry geo;                 // all R ranks
-  const uint8_t* payloads;
-  int64_t stride;
+  Geometry geo;                 // the receiver's rank range
+  const uint8_t* payloads;      // contiguous layout: range rank r at payloads + r*stride
+  const uint8_t* const* payload_ptrs;  // or (non-null) range rank r at payload_ptrs[r]
+  int64_t stride;               // slot stride, or with payload_ptrs each buffer's capacity
   const ciera_desc* descs;
   uint8_t* rcache;              // N exponent bytes
   uint16_t* out;                // N values

@@ -867,7 +867,11 @@ __global__ void __launch_bounds__(kScanThreads) k_bitmap_scan(const DecompressPa
   const int64_t bm = (nb + 7) / 8;
   const int64_t nw = (nb + 31) / 32;
   const ciera_desc d = p.descs[r];
-  const uint8_t* payload = p.payloads + static_cast<int64_t>(r) * p.stride;
+  const uint8_t* payload = payload_of(p, r);
+  // a payload from the pointer table must exist, and be 16-byte aligned for
+  // the staged path's bulk copies
+  const bool ptr_ok =
+      !p.payload_ptrs || (payload && !(p.fast && (reinterpret_cast<uintptr_t>(payload) & 15u)));
 
   // the same decision in every thread of the CTA
   uint32_t state = kRankSkip;
@@ -886,6 +890,7 @@ __global__ void __launch_bounds__(kScanThreads) k_bitmap_scan(const DecompressPa
         d.payload_bytes >= d.body_bytes && d.payload_bytes <= static_cast<uint64_t>(p.stride))
       state = kRankRans;
   }
+  if (!ptr_ok) state = kRankSkip;
   uint32_t table_bad = 0;
   if (state == kRankRans) {
     // the frequency table: no zero entry, sum 4096 (2 entries per thread)
@@ -978,7 +983,7 @@ struct DecompressShared {
 // Byte-wise tile of the receiver.
 __device__ void decompress_tile_bytes(const DecompressParams& p, const Tile& x, uint32_t state) {
   const int64_t B = p.geo.B;
-  const uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
+  const uint8_t* payload = payload_of(p, x.rl);
   uint8_t* rc = p.rcache + x.shard_off + x.e0;
   uint16_t* out = p.out + x.shard_off + x.e0;
   if (state == kRankRaw) {
@@ -1021,7 +1026,7 @@ __device__ void decompress_tile_staged(const DecompressParams& p, const Tile& x,
   uint8_t* ws = dsm;
   uint8_t* ss = dsm + 2 * TE;
   uint8_t* cs = dsm + 3 * TE;
-  const uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
+  const uint8_t* payload = payload_of(p, x.rl);
   uint8_t* rc = p.rcache + x.shard_off + x.e0;
   uint16_t* out = p.out + x.shard_off + x.e0;
   const uint32_t te = static_cast<uint32_t>(x.te);

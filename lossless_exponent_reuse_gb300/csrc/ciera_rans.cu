@@ -623,7 +623,7 @@ __global__ void __launch_bounds__(kTableThreads)
   const int64_t len = shard_len_of(p.geo, r);
   const int64_t nb = (len + p.geo.B - 1) / p.geo.B;
   const int64_t C = rans_layout(len, nb).C;
-  const uint8_t* tab = p.payloads + static_cast<int64_t>(r) * p.stride + C;
+  const uint8_t* tab = payload_of(p, r) + C;
   const uint32_t f = in_bounds(p.ctl, C + 2 * s, 2, p.stride)
                          ? tab[2 * s] | (static_cast<uint32_t>(tab[2 * s + 1]) << 8)
                          : 16u;
@@ -673,8 +673,7 @@ __global__ void __launch_bounds__(kThreads)
     // the tile's values streamed from the payload to out, their exponents to
     // the ExpCache (nothing staged)
     if (!in_bounds(p.ctl, 2 * x.e0, 2 * x.te, p.stride)) return;
-    const uint4* vs = reinterpret_cast<const uint4*>(
-        p.payloads + static_cast<int64_t>(x.rl) * p.stride + 2 * x.e0);
+    const uint4* vs = reinterpret_cast<const uint4*>(payload_of(p, x.rl) + 2 * x.e0);
     uint4* out = reinterpret_cast<uint4*>(p.out + x.shard_off + x.e0);
     uint4* rc = reinterpret_cast<uint4*>(p.rcache + x.shard_off + x.e0);
     for (int gi = tid; gi < static_cast<int>(x.te >> 4); gi += nthreads) {
@@ -694,7 +693,7 @@ __global__ void __launch_bounds__(kThreads)
   uint32_t* tabs =
       reinterpret_cast<uint32_t*>(recs + ((rans_record_stage(T, B) + 15) & ~int64_t(15)));
   const ciera_desc d = p.descs[x.rl];
-  const uint8_t* payload = p.payloads + static_cast<int64_t>(x.rl) * p.stride;
+  const uint8_t* payload = payload_of(p, x.rl);
   const RansLayout Ly = rans_layout(x.len, x.nb);
   uint8_t* rc = p.rcache + x.shard_off + x.e0;
   uint16_t* out = p.out + x.shard_off + x.e0;

@@ -72,23 +72,55 @@ def _run(wl, iterations, sampled, layer=0):
     return all_descs
 
 
-def test_workload_2_olmoe_layer():
+def _exp_change_rate(a, b):
+    return float((exps_dev(a) != exps_dev(b)).float().mean())
+
+
+def test_workload_1_matrix_all_iterations():
+    wl = workloads.workload(1)
+    descs = _run(wl, wl.iterations, sampled=[0, 1, 2, 3])
+    assert all(d["mode"] == ciera.MODE_RAW for d in descs[0])      # cold start
+
+
+def test_workload_2_olmoe_layer_all_iterations():
     wl = workloads.workload(2)
-    descs = _run(wl, 3, sampled=[0, 7, 15])
+    descs = _run(wl, wl.iterations, sampled=[0, 7, 15])
+    assert len(descs) == 10
     assert all(d["mode"] == ciera.MODE_RAW for d in descs[0])      # cold start
 
 
 def test_workload_3_warmup_and_forced_change():
     wl = workloads.workload(3)
-    descs = _run(wl, 4, sampled=[3, 12])
+    descs = _run(wl, wl.iterations, sampled=[3, 12])
     forced = descs[3]
     blocks = wl.layer_numel // wl.ranks // wl.block
     assert all(d["mode"] == ciera.MODE_RAW and d["n_changed_blocks"] == blocks for d in forced)
 
 
-def test_workload_5_finegrained_layer():
+def test_workload_5_finegrained_layer_every_rate():
+    """All 16 iterations: the cold start, then five at each step size
+    (about 0.1 %, 1 % and 10 % of exponents change), sampled ranks against
+    the oracle at every one of them."""
     wl = workloads.workload(5)
-    _run(wl, 2, sampled=[0, 31])
+    assert wl.iterations == 16
+    dev = "cuda"
+    n = wl.layer_numel
+    ag = SimulatedAllgather(n, wl.block, wl.ranks, device=dev, keep_flags=True)
+    w = workloads.initial_layer(wl, 0, dev)
+    rates = {}
+    for t in range(wl.iterations):
+        if t > 0:
+            w_new = workloads.step_layer(wl, w, 0, t)
+            rates.setdefault(wl.step_of(t), []).append(_exp_change_rate(w, w_new))
+            w = w_new
+        # ranks 0 and 31 at every iteration, one more rank that moves along
+        _check_iteration(ag, w, [0, 31, 1 + (5 * t) % 30], t, f"{wl.name} t={t}")
+    del ag, w
+    torch.cuda.empty_cache()
+    mean = {k: sum(v) / len(v) for k, v in rates.items()}
+    assert len(mean) == 3 and all(len(v) == 5 for v in rates.values())
+    lo, mid, hi = (mean[k] for k in sorted(mean))
+    assert 0.0003 < lo < 0.003 and 0.003 < mid < 0.03 and 0.03 < hi < 0.3, mean
 
 
 def test_workload_2_clustered_variant():
@@ -97,7 +129,10 @@ def test_workload_2_clustered_variant():
     assert all(d["mode"] == ciera.MODE_COMPRESSED for d in descs[2])
 
 
-def test_workload_4_layer_bucket_and_declines():
+@pytest.mark.parametrize("layer", [0, 9])
+def test_workload_4_layer_bucket_and_declines(layer):
+    """All 5 iterations of one layer's bucket of accepted tensors (layer 0
+    and layer 9 of the 16), sampled ranks against the oracle each time."""
     wl = workloads.workload(4)
     offs = workloads.layer_offsets(wl)
     accepted = [(name, o, k) for name, o, k in offs if ciera.should_compress(k)]
@@ -109,13 +144,15 @@ def test_workload_4_layer_bucket_and_declines():
     assert n == 419_430_400
     dev = "cuda"
     ag = SimulatedAllgather(n, wl.block, wl.ranks, device=dev, keep_flags=True)
-    full = workloads.initial_layer(wl, 0, dev)
-    for t in range(2):
+    full = workloads.initial_layer(wl, layer, dev)
+    for t in range(wl.iterations):
         if t > 0:
-            full = workloads.step_layer(wl, full, 0, t)
+            full = workloads.step_layer(wl, full, layer, t)
         bucket = torch.cat([full[o:o + k].view(torch.int16) for _, o, k in accepted]).view(
             torch.uint16)
-        _check_iteration(ag, bucket, [0, 7], t, f"cfg4 layer0 t={t}")
+        _check_iteration(ag, bucket, [0, 3 + t % 4, 7], t, f"cfg4 layer{layer} t={t}")
+    del ag, full, bucket
+    torch.cuda.empty_cache()
 
 
 def _run_rans(wl, iterations, sampled):

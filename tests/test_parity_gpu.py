@@ -205,18 +205,18 @@ def test_cache_invariants_and_round_trip_on_workload_2_shape_slice():
     assert torch.equal(ag.sender_cache, exps_dev(w_last))
 
 
-def test_host_streamer_round_trips_every_step():
-    # weights from pinned host memory, rebuilt weights back, overlapped
-    from lossless_exponent_reuse_gb300.allgather import HostStreamer
+def test_step_host_round_trips_every_edge_case():
+    # weights from pinned host memory, rebuilt weights back (ciera_step_host),
+    # over the edge-case sequence, in chunks of one rank
     n, R, B = 131072, 4, 256
     seq = edge_sequence(n, B, seed=21)
     ag = SimulatedAllgather(n, B, R)
-    hs = HostStreamer(ag)
+    session = ciera.HostSession(4)
+    w_dev = torch.empty(n, dtype=torch.int16, device="cuda")
     host = [torch.from_numpy(w.view(np.int16)).pin_memory() for w in seq]
     outs = [torch.empty(n, dtype=torch.int16).pin_memory() for _ in seq]
     for w, o in zip(host, outs):
-        hs.step(w, o)
-    hs.finish()
+        ag.step_host(session, w, o, w_dev, chunks=4)
     torch.cuda.synchronize()
     assert ag.status() == ciera.OK
     for w, o in zip(host, outs):
