@@ -183,20 +183,25 @@ def kernel_source_hash(kernel):
     return h.hexdigest()[:16]
 
 
-def traffic_per_value(kernel, workload):
-    """DRAM bytes per value of `kernel` on `workload` (its name without a
-    profiling cut) from profiles/traffic.md, or None if that capture was
-    taken on a different kernel source or no capture covers the workload."""
+def traffic_per_value(kernel, workload, steps):
+    """DRAM bytes per value of one launch of `kernel` on `workload` (its name
+    without a profiling cut), averaged over launches whose inputs moved by
+    the update steps `steps`, from profiles/traffic.md; None if a step has no
+    row captured on the current kernel source."""
+    rows = {}
     try:
         h = kernel_source_hash(kernel)
         for line in open(os.path.join(ROOT, "profiles", "traffic.md")):
             cells = [c.strip() for c in line.strip().strip("|").split("|")]
-            if (len(cells) >= 4 and cells[0] == kernel and cells[1] == h
+            if (len(cells) >= 5 and cells[0] == kernel and cells[1] == h
                     and cells[2] == workload):
-                return float(cells[3])
+                rows[float(cells[3])] = float(cells[4])
     except (OSError, ValueError):
-        pass
-    return None
+        return None
+    vals = [rows.get(float(st)) for st in steps]
+    if not vals or any(v is None for v in vals):
+        return None
+    return sum(vals) / len(vals)
 
 
 def instructions_per_value(kernel):
@@ -219,6 +224,15 @@ def issue_peak(device, sm_mhz):
     (four per SM) per cycle, at the SM clock sampled during the run."""
     props = torch.cuda.get_device_properties(device)
     return props.multi_processor_count * 4 * sm_mhz * 1e6
+
+
+def hold_stream(stream, k):
+    """Queue a device-side sleep on `stream` long enough for the host to
+    enqueue k steps behind it (about 0.5 ms per step at the sampled clocks),
+    so that the timed region measures the GPU and not the host's launch
+    latency."""
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(1_000_000 * (2 + k)))
 
 
 def measured_peak():
@@ -393,6 +407,9 @@ def run_ours(args, world, rank, local):
             ag.iteration -= K
         torch.cuda.synchronize()
     step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    # hold the stream on a device-side sleep (outside the timed region) while
+    # the host enqueues every timed launch, so that no step waits on the host
+    hold_stream(stream, K)
     start.record(stream)
     for i in range(K):
         step_ev[i].record(stream)
@@ -507,9 +524,11 @@ def run_ours(args, world, rank, local):
     elif rans and t_c is not None:
         dom += "+k_decompress_rans"
     base_name = workloads.workload(args.config).name
+    timed_steps = [wl.step_of(t) for t in range(W, W + K)]
     tpv = (traffic_per_value(kname if dom == kname else
                              ("k_decompress_rans" if rans else "k_decompress"),
-                             base_name + (f"_{args.variant}" if args.variant else ""))
+                             base_name + (f"_{args.variant}" if args.variant else ""),
+                             timed_steps)
            if t_c is not None else None)
     traffic = round(tpv * n) if tpv is not None else None
     # the same kernel against the copy bandwidth in the DRAM bytes ncu counted
@@ -612,6 +631,7 @@ def run_e2e(wl, seq, n, dev, world, raw_ahead=True):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
+    hold_stream(stream, K)
     start.record(stream)
     for i in range(K):
         ag.step_host(session, host[i], out_host, w_dev, chunks=chunks)
