@@ -3,7 +3,8 @@ computed offset is tested against its buffer, and one that would leave it is
 skipped and reported as CIERA_E_BOUNDS instead of touching memory.
 
 The GPU parity suites (small, random and full-size cases, graphs, the
-pipeline, the allocation-free entry point) run once more in a child process against the
+pipeline, the receiver over separate payload buffers and the host-buffer
+step, the allocation-free entry point) run once more in a child process against the
 checked library (CIERA_CHECKED=1), which must give the same bytes and no
 status."""
 import os
@@ -27,7 +28,7 @@ def test_parity_suites_under_the_checked_build():
         [sys.executable, "-m", "pytest", "-x", "-q", "-m", "gpu", "-p", "no:cacheprovider",
          "tests/test_parity_gpu.py", "tests/test_hashed_gpu.py", "tests/test_rans_gpu.py",
          "tests/test_fullsize_gpu.py", "tests/test_graph_gpu.py", "tests/test_pipeline_gpu.py",
-         "tests/test_random_gpu.py",
+         "tests/test_random_gpu.py", "tests/test_gather_host_gpu.py",
          "tests/test_zz_no_alloc.py"],
         cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
