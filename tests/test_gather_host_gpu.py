@@ -21,8 +21,10 @@ from lossless_exponent_reuse_gb300.allgather import SimulatedAllgather
 pytestmark = pytest.mark.gpu
 
 # (values, ranks, block): staged fast path, 32 blocks per tile, byte-wise
-# path with a partial last shard, empty last shards
-CASES = [(196608, 3, 4096), (131072, 4, 256), (100003, 3, 100), (40000, 7, 4096)]
+# path with a partial last shard, a short last shard of partial blocks, and
+# two empty last shards (50 values over 12 ranks of 5)
+CASES = [(196608, 3, 4096), (131072, 4, 256), (100003, 3, 100), (40000, 7, 4096),
+         (50, 12, 4)]
 
 
 def _seq(n, R, B, iters, seed, p_block=0.2):
@@ -102,19 +104,6 @@ def test_gather_skips_missing_and_misaligned_payloads():
         torch.cuda.synchronize()
         assert ag.status() == ciera.OK
         assert torch.equal(ag.out[:n].view(torch.int16), seq[1].view(torch.int16))
-
-
-def test_gather_rejects_bad_host_arguments():
-    plan = ciera.Plan(131072, 256, 4)
-    L = ciera.lib()
-    fake = 4096
-    cap = plan.info.payload_capacity
-    assert L.ciera_decompress_gather(plan.handle, None, cap, fake, fake, fake, fake, 0,
-                                     None) == ciera.E_INVAL
-    assert L.ciera_decompress_gather(plan.handle, fake + 4, cap, fake, fake, fake, fake, 0,
-                                     None) == ciera.E_INVAL        # table not 8-byte aligned
-    assert L.ciera_decompress_gather(plan.handle, fake, cap - 1, fake, fake, fake, fake, 0,
-                                     None) == ciera.E_INVAL        # short capacity
 
 
 @pytest.mark.parametrize("n,R,B", CASES)

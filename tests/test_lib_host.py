@@ -92,6 +92,26 @@ def test_compress_rejects_bad_ranges_without_touching_the_gpu():
                               None) == ciera.E_INVAL                # unknown flag
 
 
+def test_gather_and_host_step_reject_bad_arguments_without_touching_the_gpu():
+    L = ciera.lib()
+    p = ciera.Plan(1024, 256, 4)
+    cap = p.info.payload_capacity
+    fake = ctypes.c_void_p(4096)     # never dereferenced: the checks fail first
+    gather = lambda table, capacity, flags: L.ciera_decompress_gather(
+        p.handle, table, capacity, fake, fake, fake, fake, flags, None)
+    assert gather(None, cap, 0) == ciera.E_INVAL                      # no pointer table
+    assert gather(ctypes.c_void_p(4100), cap, 0) == ciera.E_INVAL     # table not 8-byte aligned
+    assert gather(fake, cap - 1, 0) == ciera.E_INVAL                  # short capacity
+    assert gather(fake, cap, 2) == ciera.E_INVAL                      # unknown flag
+    h = ctypes.c_void_p()
+    assert L.ciera_host_session_create(0, ctypes.byref(h)) == ciera.E_INVAL
+    assert L.ciera_host_session_create(4, None) == ciera.E_INVAL
+    host = ctypes.c_void_p(8192)
+    assert L.ciera_step_host(None, p.handle, host, host, fake, fake, fake, cap, fake, fake, fake,
+                             fake, 0, 1, None) == ciera.E_INVAL       # no session
+    L.ciera_host_session_destroy(None)                                # NULL is ignored
+
+
 def test_predicate_matches_oracle():
     for n in [0, 1, 2047, 2048, 131072, 200000, 206000, 206300, 207000, 2097152, 4194304,
               10**9]:
