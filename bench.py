@@ -64,9 +64,15 @@ def parse_args():
     ap.add_argument("--sender", choices=["exact", "hash", "rans"], default="exact",
                     help="change test: exact exponent compare (default) or the 128-bit "
                          "block hash with a 16-byte-per-block HashCache")
-    ap.add_argument("--no-raw-ahead", action="store_true",
-                    help="exact/hash senders: every shard takes the look-back scan, "
-                         "even those predicted raw")
+    ra = ap.add_mutually_exclusive_group()
+    ra.add_argument("--raw-ahead", dest="raw_ahead", action="store_true", default=None,
+                    help="exact/hash senders: shards whose last payload was RAW skip the "
+                         "look-back (default for the hashed sender)")
+    ra.add_argument("--no-raw-ahead", dest="raw_ahead", action="store_false",
+                    help="exact/hash senders: every shard takes the look-back scan (default "
+                         "for the exact sender, whose look-back tiles prefetch the tiles "
+                         "ahead into L2 and run as fast, and which then never rewrites a "
+                         "shard whose prediction failed)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=4,
                     help="end-to-end leg: distinct iterations held in pinned host memory "
@@ -361,7 +367,7 @@ def run_ours(args, world, rank, local):
     gen = iteration_buckets(wl, W + K, dev)
     hashed = args.sender == "hash"
     rans = args.sender == "rans"
-    raw_ahead = not args.no_raw_ahead
+    raw_ahead = args.raw_ahead if args.raw_ahead is not None else hashed
     layers = [SimulatedAllgather(n, wl.block, wl.ranks, device=dev, hashed=hashed, rans=rans,
                                  raw_ahead=raw_ahead)
               for _ in range(L)]
