@@ -353,6 +353,34 @@ def cpu_baseline(wl, seq_host, warm_t, budget_s):
                       f"compress+decompress, one rank per thread"}
 
 
+L2_BYTES = 129 * 1000 * 1000   # GB300 L2
+
+
+def raw_ahead_of(args):
+    """Raw-ahead setting of the exact/hashed senders: as asked, else off for
+    the exact sender and on for the hashed one."""
+    return args.raw_ahead if args.raw_ahead is not None else args.sender == "hash"
+
+
+def arm_config(args, wl, n, declined, world):
+    """The `config` object of the JSON line, the same for both arms: the
+    workload, its sizes and the timed iterations."""
+    W, K = args.warmup, args.steps
+    cfg = {"workload": wl.name, "sender": args.sender, "schedule": args.schedule,
+           "numel": n * wl.layers, "layers": wl.layers, "numel_per_plan": n,
+           "ranks": wl.ranks, "block": wl.block, "step": wl.steps[0],
+           "iterations_timed": f"{W}..{W + K - 1}", "parallelism": f"replicas{world}",
+           "l2": (f"inputs larger than L2 ({2 * n / 1e6:.0f} MB of weights per plan), no flush"
+                  if 2 * n > L2_BYTES else
+                  f"inputs smaller than L2 ({2 * n / 1e6:.1f} MB of weights per plan): "
+                  f"not a bench-line workload")}
+    if declined:
+        cfg["declined_values_per_layer"] = declined
+    if args.sender != "rans":
+        cfg["raw_ahead"] = bool(raw_ahead_of(args))
+    return cfg
+
+
 def run_ours(args, world, rank, local):
     from lossless_exponent_reuse_gb300 import ciera, workloads
     from lossless_exponent_reuse_gb300.allgather import SimulatedAllgather
@@ -367,7 +395,7 @@ def run_ours(args, world, rank, local):
     gen = iteration_buckets(wl, W + K, dev)
     hashed = args.sender == "hash"
     rans = args.sender == "rans"
-    raw_ahead = args.raw_ahead if args.raw_ahead is not None else hashed
+    raw_ahead = raw_ahead_of(args)
     layers = [SimulatedAllgather(n, wl.block, wl.ranks, device=dev, hashed=hashed, rans=rans,
                                  raw_ahead=raw_ahead)
               for _ in range(L)]
@@ -545,18 +573,13 @@ def run_ours(args, world, rank, local):
     # (algorithmic bytes count every changed value's cache refresh, which the
     # kernel writes only for the 16-byte groups that differ)
     dram_gbs = traffic / (dom_ms / 1e3) / 1e9 if traffic is not None else None
-    cfg = {"workload": wl.name, "sender": args.sender, "schedule": sched, "numel": n * L,
-           "layers": L,
-           "numel_per_plan": n,
-           "ranks": wl.ranks, "block": wl.block, "step": wl.steps[0],
-           "iterations_timed": f"{W}..{W + K - 1}", "parallelism": f"replicas{world}",
-           "l2": f"inputs larger than L2 ({2 * n / 1e6:.0f} MB of weights per plan), no flush"}
-    if declined:
-        cfg["declined_values_per_layer"] = declined
+    cfg = arm_config(args, wl, n, declined, world)
     info0 = layers[0].plan.info
+    # raw-ahead takes effect on staged plans of at most 32 blocks per tile
+    # (every workload here), which then launch k_repack as well
     repack = int(raw_ahead and not rans and bool(info0.fast_path) and info0.tile_blocks <= 32)
-    if not rans:
-        cfg["raw_ahead"] = bool(repack)
+    if not rans and raw_ahead and not repack:
+        cfg["raw_ahead"] = False
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(total_s * 1e3 / K, 4),
@@ -701,15 +724,23 @@ def run_reference(args, world, rank):
     wl = workloads.workload(args.config, args.variant)
     n, R, B = wl.layer_numel, wl.ranks, wl.block
     W, K = args.warmup, args.steps
+    # the workload as the other arm names it: the tensors the per-tensor
+    # predicate takes (the oracle's restatement of it)
+    offs = workloads.layer_offsets(wl)
+    n_acc = sum(k for _, o, k in offs if oracle.should_compress(k))
+    cfg = arm_config(args, wl, n_acc, sum(k for _, o, k in offs) - n_acc, world)
     # each step: one rank's shard of one iteration, compress + decompress
     S = oracle.shard_size(n, R)
     # input generation only (not timed): on the GPU when there is one, since
     # a 2.4 G-value layer draws slowly on the host; rank 0's shard is kept
     gdev = "cuda" if torch.cuda.is_available() else "cpu"
     from lossless_exponent_reuse_gb300 import workloads as _wl
+    # the same iterations as the other arm: 0 is the cold start, 1 .. W-1
+    # warm up, W .. W+K-1 are timed
+    W0 = max(W, 1)
     seq_host = []
     w = _wl.initial_layer(wl, 0, gdev)
-    for t in range(W + K + 1):
+    for t in range(W0 + K):
         if t > 0:
             w = _wl.step_layer(wl, w, 0, t)
         seq_host.append(w[:S].view(torch.int16).cpu().numpy().view(np.uint16).copy())
@@ -717,14 +748,12 @@ def run_reference(args, world, rank):
     threads = 1
     sc = np.zeros(S, np.uint8)
     rc = np.zeros(S, np.uint8)
-    p, _, d = oracle.compress_shard(seq_host[0][:S], B, sc, True)
-    oracle.decompress_shard(p, d, S, B, rc)
-    for t in range(1, W + 1):
-        p, _, d = oracle.compress_shard(seq_host[t][:S], B, sc, False)
+    for t in range(W0):
+        p, _, d = oracle.compress_shard(seq_host[t], B, sc, t == 0)
         oracle.decompress_shard(p, d, S, B, rc)
     t0 = time.perf_counter()
-    for i in range(K):
-        p, _, d = oracle.compress_shard(seq_host[W + 1 + i][:S], B, sc, False)
+    for t in range(W0, W0 + K):
+        p, _, d = oracle.compress_shard(seq_host[t], B, sc, False)
         st, _ = oracle.decompress_shard(p, d, S, B, rc)
         assert st == 0
     dt = time.perf_counter() - t0
@@ -733,12 +762,11 @@ def run_reference(args, world, rank):
             "steps": K, "warmup": W, "ms_per_step": round(dt * 1e3 / K, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": wl.name, "numel": n, "ranks": R, "block": B,
-                       "sample": f"rank 0 shard ({S} values) per step"},
+            "config": cfg,
             "cpu_baseline": {"value": round(val, 4), "unit": UNIT, "cores": threads,
                              "kind": "oracle",
-                             "sample": f"rank 0 shard of iterations {W + 1}..{W + K}, "
-                                       f"compress+decompress"},
+                             "sample": f"rank 0 shard ({S} values of layer 0) of iterations "
+                                       f"{W0}..{W0 + K - 1}, compress+decompress, one step each"},
             "e2e": {"value": round(val, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
