@@ -67,12 +67,11 @@ def parse_args():
     ra = ap.add_mutually_exclusive_group()
     ra.add_argument("--raw-ahead", dest="raw_ahead", action="store_true", default=None,
                     help="exact/hash senders: shards whose last payload was RAW skip the "
-                         "look-back (default for the hashed sender)")
+                         "look-back (default for the hashed sender and for the pipelined "
+                         "and graph schedules)")
     ra.add_argument("--no-raw-ahead", dest="raw_ahead", action="store_false",
                     help="exact/hash senders: every shard takes the look-back scan (default "
-                         "for the exact sender, whose look-back tiles prefetch the tiles "
-                         "ahead into L2 and run as fast, and which then never rewrites a "
-                         "shard whose prediction failed)")
+                         "for the exact sender on the sequential schedule)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=4,
                     help="end-to-end leg: distinct iterations held in pinned host memory "
@@ -357,9 +356,15 @@ L2_BYTES = 129 * 1000 * 1000   # GB300 L2
 
 
 def raw_ahead_of(args):
-    """Raw-ahead setting of the exact/hashed senders: as asked, else off for
-    the exact sender and on for the hashed one."""
-    return args.raw_ahead if args.raw_ahead is not None else args.sender == "hash"
+    """Raw-ahead setting of the exact/hashed senders: as asked, else on for
+    the hashed sender and for the overlapped schedules, off for the exact
+    sender run layer by layer.  The exact sender's look-back tiles prefetch
+    the tiles ahead into L2 and run as fast alone, and never rewrite a shard
+    whose prediction failed; next to a receiver on the other stream they
+    cost it bandwidth."""
+    if args.raw_ahead is not None:
+        return args.raw_ahead
+    return args.sender == "hash" or args.schedule != "sequential"
 
 
 def arm_config(args, wl, n, declined, world):
