@@ -693,31 +693,35 @@ def run_e2e(wl, seq, n, dev, world, raw_ahead=True):
             "link_bound": round(link, 2), "frac_of_link": round(val / link, 4)}
 
 
-def link_bound(host, out_host, w_dev, stream):
+def link_bound(host, out_host, w_dev, stream, reps=3):
     """bf16 GB/s that the host link alone sustains for the e2e traffic: each
     step uploads one input (pinned) and downloads one output of the same size,
-    on two streams at the same time, with no kernel.  The e2e figure divided
-    by this is the share of the link the path uses; boxes differ in this
-    bound, the kernels do not."""
+    on two streams at the same time, with no kernel.  The best of `reps`
+    passes, since other traffic on a shared host link can only slow a pass
+    down.  The e2e figure divided by this is the share of the link the path
+    uses; boxes differ in this bound, the kernels do not."""
     n = host[0].numel()
     K = len(host)
     src = torch.empty(n, dtype=torch.int16, device=w_dev.device)
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    start.record(stream)
-    s_in.wait_stream(stream)
-    s_out.wait_stream(stream)
-    for i in range(K):
-        with torch.cuda.stream(s_in):
-            w_dev[:n].copy_(host[i], non_blocking=True)
-        with torch.cuda.stream(s_out):
-            out_host.copy_(src, non_blocking=True)
-    stream.wait_stream(s_in)
-    stream.wait_stream(s_out)
-    end.record(stream)
-    torch.cuda.synchronize()
-    return 2.0 * n * K / (start.elapsed_time(end) / 1e3) / 1e9
+    best = 0.0
+    for _ in range(reps):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        start.record(stream)
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for i in range(K):
+            with torch.cuda.stream(s_in):
+                w_dev[:n].copy_(host[i], non_blocking=True)
+            with torch.cuda.stream(s_out):
+                out_host.copy_(src, non_blocking=True)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+        end.record(stream)
+        torch.cuda.synchronize()
+        best = max(best, 2.0 * n * K / (start.elapsed_time(end) / 1e3) / 1e9)
+    return best
 
 
 def run_reference(args, world, rank):
