@@ -190,19 +190,21 @@ def kernel_source_hash(kernel):
     return h.hexdigest()[:16]
 
 
-def traffic_per_value(kernel, workload, steps):
+def traffic_per_value(kernel, workload, steps, raw_ahead):
     """DRAM bytes per value of one launch of `kernel` on `workload` (its name
     without a profiling cut), averaged over launches whose inputs moved by
-    the update steps `steps`, from profiles/traffic.md; None if a step has no
-    row captured on the current kernel source."""
+    the update steps `steps`, from profiles/traffic.md; rows are taken with
+    the sender's raw-ahead setting ("on"/"off") or for either ("-").  None if
+    a step has no row captured on the current kernel source."""
     rows = {}
+    setting = "on" if raw_ahead else "off"
     try:
         h = kernel_source_hash(kernel)
         for line in open(os.path.join(ROOT, "profiles", "traffic.md")):
             cells = [c.strip() for c in line.strip().strip("|").split("|")]
-            if (len(cells) >= 5 and cells[0] == kernel and cells[1] == h
-                    and cells[2] == workload):
-                rows[float(cells[3])] = float(cells[4])
+            if (len(cells) >= 6 and cells[0] == kernel and cells[1] == h
+                    and cells[2] == workload and cells[3] in ("-", setting)):
+                rows[float(cells[4])] = float(cells[5])
     except (OSError, ValueError):
         return None
     vals = [rows.get(float(st)) for st in steps]
@@ -571,7 +573,7 @@ def run_ours(args, world, rank, local):
     tpv = (traffic_per_value(kname if dom == kname else
                              ("k_decompress_rans" if rans else "k_decompress"),
                              base_name + (f"_{args.variant}" if args.variant else ""),
-                             timed_steps)
+                             timed_steps, raw_ahead and not rans)
            if t_c is not None else None)
     traffic = round(tpv * n) if tpv is not None else None
     # the same kernel against the copy bandwidth in the DRAM bytes ncu counted
