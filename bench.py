@@ -72,6 +72,12 @@ def parse_args():
     ra.add_argument("--no-raw-ahead", dest="raw_ahead", action="store_false",
                     help="exact/hash senders: every shard takes the look-back scan (default "
                          "for the exact sender on the sequential schedule)")
+    ap.add_argument("--per-iteration", action="store_true",
+                    help="report instead of the bench line: every iteration of the workload "
+                         "after the cold start, each kernel timed alone from the same cache "
+                         "state after an L2 flush, median of --reps; one JSON line per "
+                         "iteration (one GPU)")
+    ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=4,
                     help="end-to-end leg: distinct iterations held in pinned host memory "
@@ -726,6 +732,98 @@ def link_bound(host, out_host, w_dev, stream, reps=3):
     return best
 
 
+def run_per_iteration(args, world, local):
+    """Per-iteration report: for every iteration t >= 1 of the workload as
+    written (iteration 0 is the cold start), each layer's compress and
+    gather-decompress are timed alone, --reps times, each time from the
+    state left by iteration t-1 (caches, workspace and RANS histograms
+    restored untimed) and after a 512 MB write that flushes L2; the medians
+    are reported with the iteration's measured exponent change rate, changed
+    fraction f, wire bytes and payload modes.  Every repetition must rebuild
+    the iteration exactly."""
+    from lossless_exponent_reuse_gb300 import ciera, workloads
+    from lossless_exponent_reuse_gb300.allgather import SimulatedAllgather
+    if world != 1:
+        raise SystemExit("--per-iteration runs on one GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = workloads.workload(args.config, args.variant)
+    acc, _ = accepted_tensors(wl)
+    n = sum(k for _, k in acc)
+    if n == 0:
+        print(json.dumps({"report": "per_iteration", "workload": wl.name,
+                          "note": "the per-tensor predicate declines every tensor"}))
+        return
+    L = wl.layers
+    hashed, rans = args.sender == "hash", args.sender == "rans"
+    raw_ahead = raw_ahead_of(args)
+    layers = [SimulatedAllgather(n, wl.block, wl.ranks, device=dev, hashed=hashed, rans=rans,
+                                 raw_ahead=raw_ahead)
+              for _ in range(L)]
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    def state(ag):
+        return ([ag.hash_cache if hashed else ag.sender_cache, ag.recv_cache, ag.workspace] +
+                (list(ag.hist) if rans else []))
+
+    gen = iteration_buckets(wl, wl.iterations, dev)
+    prev = next(gen)
+    for ag, w in zip(layers, prev):
+        ag.step(w)                                   # iteration 0: the cold start
+    for t in range(1, wl.iterations):
+        cur = next(gen)
+        tc, td, bc, bd, fsum, wire, modes = 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, {}
+        for ag, w in zip(layers, cur):
+            snap = [x.clone() for x in state(ag)]
+            it = ag.iteration
+            c_ms, d_ms = [], []
+            for r in range(args.reps):
+                for x, x0 in zip(state(ag), snap):
+                    x.copy_(x0)
+                ag.iteration = it
+                flush.fill_(r & 0xFF)
+                ev[0].record(stream)
+                ag.compress(w)
+                ev[1].record(stream)
+                flush.fill_((r + 1) & 0xFF)
+                ev[2].record(stream)
+                ag.decompress()
+                ev[3].record(stream)
+                torch.cuda.synchronize()
+                c_ms.append(ev[0].elapsed_time(ev[1]))
+                d_ms.append(ev[2].elapsed_time(ev[3]))
+                if ag.status() != ciera.OK or not torch.equal(ag.out[:n].view(torch.int16),
+                                                              w.view(torch.int16)):
+                    raise RuntimeError(f"iteration {t}: not rebuilt exactly")
+            del snap
+            tc += statistics.median(c_ms)
+            td += statistics.median(d_ms)
+            descs = ag.descriptors()
+            c_, d_, f_ = algorithmic_bytes(descs, n, hashed, wl.block)
+            bc, bd, fsum = bc + c_, bd + d_, fsum + f_
+            wire += sum(d["payload_bytes"] for d in descs)
+            for d in descs:
+                modes[d["mode"]] = modes.get(d["mode"], 0) + 1
+        changed = sum(int(torch.count_nonzero((a.view(torch.int16) ^ b.view(torch.int16))
+                                              & 0x7F80)) for a, b in zip(prev, cur))
+        peak, _ = measured_peak()
+        print(json.dumps({
+            "report": "per_iteration", "workload": wl.name, "sender": args.sender,
+            "raw_ahead": bool(raw_ahead) if not rans else None, "iteration": t,
+            "step": wl.step_of(t), "forced": t in wl.forced, "numel": n * L, "reps": args.reps, "l2": "flushed (512 MB write)",
+            "compress_ms": round(tc, 4), "decompress_ms": round(td, 4),
+            "bf16_gbs": round(2.0 * n * L / ((tc + td) / 1e3) / 1e9, 1),
+            "hbm_frac": round((bc + bd) / ((tc + td) / 1e3) / 1e9 / peak, 4),
+            "exponent_change_rate": round(changed / (n * L), 6),
+            "changed_fraction": round(fsum / L, 4),
+            "wire_bytes_per_value": round(wire / (n * L), 4),
+            "modes": {{0: "compressed", 1: "raw", 2: "rans"}[k]: v
+                      for k, v in sorted(modes.items())}}), flush=True)
+        prev = cur
+
+
 def run_reference(args, world, rank):
     """The oracle as the reference arm: on the host cores, bounded samples."""
     if rank != 0:
@@ -787,7 +885,10 @@ def main():
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
     world, rank, local = dist_setup()
-    if args.impl == "reference":
+    if args.per_iteration and args.impl == "ours":
+        run_per_iteration(args, world, local)
+        res = None
+    elif args.impl == "reference":
         res = run_reference(args, world, rank)
     else:
         res = run_ours(args, world, rank, local)
