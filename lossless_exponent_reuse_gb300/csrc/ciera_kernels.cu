@@ -137,10 +137,18 @@ __device__ __forceinline__ void flag_sync(int nf) {
 // the GPU), unless that tile's shard is predicted raw.  A tile that waits on
 // its look-back holds its staging, so fewer loads are in flight; the lines
 // brought in ahead keep DRAM busy meanwhile, and the later tile's bulk copies
-// find them in L2.  Much further ahead the lines are evicted before use.
+// find them in L2.  The prefetch is one bulk request per range, marked
+// evict_last so that the lines outlast the stream of payload and cache
+// writes until their tile loads them.  Much further ahead they are evicted
+// before use all the same.
 constexpr int64_t kPrefetchAhead = 512;
-__device__ __forceinline__ void prefetch_l2(const void* a) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+// [a, a + bytes) into L2: a 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* a, uint32_t bytes) {
+  unsigned long long policy;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(a),
+               "r"(bytes), "l"(policy)
+               : "memory");
 }
 
 // Block of 16-value group gi on the staged paths (blocks of G = B/16 >= 16
@@ -476,18 +484,15 @@ __global__ void __launch_bounds__(kThreads, 9) k_compress(const CompressParams p
     sh.ahead = p.raw_ahead && (x.len & 15) == 0 && (cold || __ldg(p.pred + x.rl) != 0u);
   }
   __syncthreads();
-  if (!kHashed && stg && g + kPrefetchAhead < p.geo.total_tiles) {
+  if (!kHashed && stg && tid == 0 && g + kPrefetchAhead < p.geo.total_tiles) {
     const Tile y = decode_ticket(p.geo, g + kPrefetchAhead);
     const bool y_ahead =
         p.raw_ahead && (y.len & 15) == 0 && (cold || __ldg(p.pred + y.rl) != 0u);
-    if (!y_ahead) {
-      // 128-byte lines wholly inside the tile's values, then its cached exponents
-      const char* wy = reinterpret_cast<const char*>(p.w + y.shard_off + y.e0);
-      const char* cy = reinterpret_cast<const char*>(p.scache + y.shard_off + y.e0);
-      const int nw = static_cast<int>((2 * y.te) >> 7), nc = static_cast<int>(y.te >> 7);
-      for (int i = tid; i < nw + nc; i += blockDim.x)
-        prefetch_l2(i < nw ? wy + 128 * static_cast<int64_t>(i)
-                           : cy + 128 * static_cast<int64_t>(i - nw));
+    // staged plans keep every shard and block start 16-byte aligned; a
+    // ragged last tile of a partial shard is left to its own copy
+    if (!y_ahead && (y.te & 15) == 0) {
+      prefetch_l2_bulk(p.w + y.shard_off + y.e0, static_cast<uint32_t>(2 * y.te));
+      prefetch_l2_bulk(p.scache + y.shard_off + y.e0, static_cast<uint32_t>(y.te));
     }
   }
 
