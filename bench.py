@@ -654,13 +654,16 @@ def run_ours(args, world, rank, local):
     return result
 
 
-def run_e2e(wl, seq, n, dev, world, raw_ahead=True):
+def run_e2e(wl, seq, n, dev, world, raw_ahead=True, passes=3):
     """The same metric through the C ABI with host buffers: each step is one
     ciera_step_host call, which copies that step's weights from pinned host
     memory, runs the sender and the gather-decompress, and copies the rebuilt
     weights back, in chunks of ranks whose copies overlap the kernels.  A
     fresh state is warmed up on the inputs first (the first call is the cold
-    start); then every input is timed once, in order."""
+    start); then every input is timed once, in order, in each of `passes`
+    passes.  The value is the best pass (all are listed): the host link is
+    shared with the other GPUs of the node, whose traffic can only slow a
+    pass down, and link_bound is taken the same way."""
     from lossless_exponent_reuse_gb300 import ciera
     from lossless_exponent_reuse_gb300.allgather import SimulatedAllgather
     K = len(seq)
@@ -676,25 +679,29 @@ def run_e2e(wl, seq, n, dev, world, raw_ahead=True):
     for t in range(min(3, K)):                        # warm-up (first call is the cold start)
         ag.step_host(session, host[t], out_host, w_dev, chunks=chunks)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    hold_stream(stream, K)
-    start.record(stream)
-    for i in range(K):
-        ag.step_host(session, host[i], out_host, w_dev, chunks=chunks)
-    end.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    if ag.status() != ciera.OK:
-        raise RuntimeError("e2e steps reported an error status")
-    if not torch.equal(out_host, host[K - 1]):
-        raise RuntimeError("e2e round trip is not exact")
-    t = max_over_ranks(world, start.elapsed_time(end) / 1e3)
-    val = 2.0 * sum_over_ranks(world, float(n * K)) / t / 1e9
+    vals = []
+    for _ in range(passes):
+        barrier(world)
+        torch.cuda.synchronize()
+        hold_stream(stream, K)
+        start.record(stream)
+        for i in range(K):
+            ag.step_host(session, host[i], out_host, w_dev, chunks=chunks)
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        if ag.status() != ciera.OK:
+            raise RuntimeError("e2e steps reported an error status")
+        if not torch.equal(out_host, host[K - 1]):
+            raise RuntimeError("e2e round trip is not exact")
+        t = max_over_ranks(world, start.elapsed_time(end) / 1e3)
+        vals.append(2.0 * sum_over_ranks(world, float(n * K)) / t / 1e9)
+    val = max(vals)
     del ag
     link = link_bound(host, out_host, w_dev, stream)
     return {"value": round(val, 2), "unit": UNIT, "h2d_bytes_per_step": 2 * n,
             "d2h_bytes_per_step": 2 * n, "steps": K, "chunks": chunks,
+            "passes": [round(v, 2) for v in vals],
             "api": "ciera_step_host (C ABI, pinned host buffers)",
             # the same bytes moved by plain copies alone, both directions at
             # once on two streams: what this machine's host link allows
