@@ -698,23 +698,26 @@ def run_e2e(wl, seq, n, dev, world, raw_ahead=True, passes=3):
         vals.append(2.0 * sum_over_ranks(world, float(n * K)) / t / 1e9)
     val = max(vals)
     del ag
-    link = link_bound(host, out_host, w_dev, stream)
+    per = -(-wl.ranks // chunks)                     # ranks per chunk, as ciera_step_host
+    link = link_bound(host, out_host, w_dev, stream, per * (-(-n // wl.ranks)))
     return {"value": round(val, 2), "unit": UNIT, "h2d_bytes_per_step": 2 * n,
             "d2h_bytes_per_step": 2 * n, "steps": K, "chunks": chunks,
             "passes": [round(v, 2) for v in vals],
             "api": "ciera_step_host (C ABI, pinned host buffers)",
-            # the same bytes moved by plain copies alone, both directions at
-            # once on two streams: what this machine's host link allows
+            # the same bytes in the same chunks moved by plain copies alone,
+            # both directions at once on two streams: what this machine's host
+            # link allows
             "link_bound": round(link, 2), "frac_of_link": round(val / link, 4)}
 
 
-def link_bound(host, out_host, w_dev, stream, reps=3):
+def link_bound(host, out_host, w_dev, stream, chunk, reps=3):
     """bf16 GB/s that the host link alone sustains for the e2e traffic: each
-    step uploads one input (pinned) and downloads one output of the same size,
-    on two streams at the same time, with no kernel.  The best of `reps`
-    passes, since other traffic on a shared host link can only slow a pass
-    down.  The e2e figure divided by this is the share of the link the path
-    uses; boxes differ in this bound, the kernels do not."""
+    step uploads one input (pinned) and downloads one output of the same
+    size, cut into the same chunks of `chunk` values as ciera_step_host
+    cuts them, on two streams at the same time, with no kernel.  The best
+    of `reps` passes, since other traffic on a shared host link can only
+    slow a pass down.  The e2e figure divided by this is the share of the
+    link the path uses; boxes differ in this bound, the kernels do not."""
     n = host[0].numel()
     K = len(host)
     src = torch.empty(n, dtype=torch.int16, device=w_dev.device)
@@ -727,10 +730,12 @@ def link_bound(host, out_host, w_dev, stream, reps=3):
         s_in.wait_stream(stream)
         s_out.wait_stream(stream)
         for i in range(K):
-            with torch.cuda.stream(s_in):
-                w_dev[:n].copy_(host[i], non_blocking=True)
-            with torch.cuda.stream(s_out):
-                out_host.copy_(src, non_blocking=True)
+            for a in range(0, n, chunk):
+                b = min(n, a + chunk)
+                with torch.cuda.stream(s_in):
+                    w_dev[a:b].copy_(host[i][a:b], non_blocking=True)
+                with torch.cuda.stream(s_out):
+                    out_host[a:b].copy_(src[a:b], non_blocking=True)
         stream.wait_stream(s_in)
         stream.wait_stream(s_out)
         end.record(stream)
