@@ -132,15 +132,16 @@ __device__ __forceinline__ void flag_sync(int nf) {
   asm volatile("bar.sync 1, %0;" ::"r"(nf) : "memory");
 }
 
-// A compress CTA sends to L2 the values and cached exponents of the tile
-// kPrefetchAhead tickets after its own (about a third of the CTAs resident on
-// the GPU), unless that tile's shard is predicted raw.  A tile that waits on
-// its look-back holds its staging, so fewer loads are in flight; the lines
-// brought in ahead keep DRAM busy meanwhile, and the later tile's bulk copies
-// find them in L2.  The prefetch is one bulk request per range, marked
-// evict_last so that the lines outlast the stream of payload and cache
-// writes until their tile loads them.  Much further ahead they are evicted
-// before use all the same.
+// A compress CTA sends to L2 the values and cached exponents (the hashed
+// sender: the HashCache entries) of the tile kPrefetchAhead tickets after its
+// own (about a third of the CTAs resident on the GPU), unless that tile's
+// shard is predicted raw.  A tile that waits on its look-back holds its
+// staging, so fewer loads are in flight; the lines brought in ahead keep DRAM
+// busy meanwhile, and the later tile's bulk copies find them in L2.  The
+// prefetch is one bulk request per range, from one thread, marked evict_last
+// so that the lines outlast the stream of payload and cache writes until
+// their tile loads them.  Much further ahead they are evicted before use all
+// the same.
 constexpr int64_t kPrefetchAhead = 512;
 // [a, a + bytes) into L2: a 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* a, uint32_t bytes) {
@@ -484,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 9) k_compress(const CompressParams p
     sh.ahead = p.raw_ahead && (x.len & 15) == 0 && (cold || __ldg(p.pred + x.rl) != 0u);
   }
   __syncthreads();
-  if (!kHashed && stg && tid == 0 && g + kPrefetchAhead < p.geo.total_tiles) {
+  if (stg && tid == 0 && g + kPrefetchAhead < p.geo.total_tiles) {
     const Tile y = decode_ticket(p.geo, g + kPrefetchAhead);
     const bool y_ahead =
         p.raw_ahead && (y.len & 15) == 0 && (cold || __ldg(p.pred + y.rl) != 0u);
@@ -492,7 +493,11 @@ __global__ void __launch_bounds__(kThreads, 9) k_compress(const CompressParams p
     // ragged last tile of a partial shard is left to its own copy
     if (!y_ahead && (y.te & 15) == 0) {
       prefetch_l2_bulk(p.w + y.shard_off + y.e0, static_cast<uint32_t>(2 * y.te));
-      prefetch_l2_bulk(p.scache + y.shard_off + y.e0, static_cast<uint32_t>(y.te));
+      if (kHashed)
+        prefetch_l2_bulk(p.hash_cache + 2 * (static_cast<int64_t>(y.rl) * p.hash_stride + y.k0),
+                         static_cast<uint32_t>(16 * y.nblk));
+      else
+        prefetch_l2_bulk(p.scache + y.shard_off + y.e0, static_cast<uint32_t>(y.te));
     }
   }
 
