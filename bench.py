@@ -672,7 +672,7 @@ def run_e2e(wl, seq, n, dev, world, raw_ahead=True, passes=3):
     torch.cuda.empty_cache()
     out_host = torch.empty(n, dtype=torch.int16).pin_memory()
     w_dev = torch.empty(n, dtype=torch.int16, device=dev)
-    chunks = min(wl.ranks, 16)
+    chunks = wl.ranks                                 # one rank per chunk
     ag = SimulatedAllgather(n, wl.block, wl.ranks, device=dev, raw_ahead=raw_ahead)
     session = ciera.HostSession(chunks)
     stream = torch.cuda.current_stream()
