@@ -424,6 +424,12 @@ def run_ours(args, world, rank, local):
         del buckets
     if any(ag.status() != ciera.OK for ag in layers):
         raise RuntimeError("warm-up reported an error status")
+    # the K timed inputs stay resident in HBM; say so plainly if they cannot
+    need = 2 * n * L * K + (2 << 30)
+    free = torch.cuda.mem_get_info(dev)[0]
+    if need > free:
+        raise SystemExit(f"{K} timed steps of this workload hold {need / 1e9:.0f} GB of inputs "
+                         f"in HBM and {free / 1e9:.0f} GB are free: take fewer --steps")
     seq = [next(gen) for _ in range(K)]             # timed inputs, resident in HBM
     if want_cpu:
         warm_host.append(seq[0][0].view(torch.int16).cpu().numpy().view(np.uint16))
