@@ -75,3 +75,18 @@ def test_traffic_rows_follow_the_raw_ahead_setting(tmp_path, monkeypatch):
     # rows marked "-" serve either setting; rows of other kernel code never
     assert bench.traffic_per_value("k_compress", "v", [0.1], True) == 3.0
     assert bench.traffic_per_value("k_compress", "v", [0.2], False) is None
+
+
+def test_default_bench_line_has_dram_traffic_for_the_current_kernels():
+    """profiles/traffic.md holds rows captured on the current kernel code for
+    the default workload's timed iterations, so the default bench line carries
+    roofline.traffic and frac_dram."""
+    args = _args()
+    wl = workloads.workload(args.config, args.variant)
+    steps = [wl.step_of(t) for t in range(args.warmup, args.warmup + args.steps)]
+    raw_ahead = bench.raw_ahead_of(args)
+    assert bench.traffic_per_value("k_compress", wl.name, steps, raw_ahead) is not None
+    assert bench.traffic_per_value("k_decompress", wl.name, steps, raw_ahead) is not None
+    # the driver's 20 steps after 5 warm-ups wrap the rates once: still covered
+    steps20 = [wl.step_of(t) for t in range(5, 25)]
+    assert bench.traffic_per_value("k_compress", wl.name, steps20, raw_ahead) is not None
