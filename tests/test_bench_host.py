@@ -87,6 +87,6 @@ def test_default_bench_line_has_dram_traffic_for_the_current_kernels():
     raw_ahead = bench.raw_ahead_of(args)
     assert bench.traffic_per_value("k_compress", wl.name, steps, raw_ahead) is not None
     assert bench.traffic_per_value("k_decompress", wl.name, steps, raw_ahead) is not None
-    # the driver's 20 steps after 5 warm-ups wrap the rates once: still covered
+    # 20 steps after 5 warm-ups wrap the rates once: still covered
     steps20 = [wl.step_of(t) for t in range(5, 25)]
     assert bench.traffic_per_value("k_compress", wl.name, steps20, raw_ahead) is not None
