@@ -356,6 +356,8 @@ def cpu_baseline(wl, seq_host, warm_t, budget_s):
         dt = time.perf_counter() - t0
     return {"value": round(2.0 * done / dt / 1e9, 4), "unit": UNIT,
             "cores": min(threads, ranks), "kind": "oracle",
+            # host time per value and core: compress + decompress of one value
+            "ns_per_value_core": round(dt * 1e9 * min(threads, ranks) / done, 2),
             "sample": f"one iteration of {ranks}/{R} ranks of one plan ({done} values), "
                       f"compress+decompress, one rank per thread"}
 
@@ -899,6 +901,7 @@ def run_reference(args, world, rank):
             "config": cfg,
             "cpu_baseline": {"value": round(val, 4), "unit": UNIT, "cores": threads,
                              "kind": "oracle",
+                             "ns_per_value_core": round(dt * 1e9 / (S * K), 2),
                              "sample": f"rank 0 shard ({S} values of layer 0) of iterations "
                                        f"{W0}..{W0 + K - 1}, compress+decompress, one step each"},
             "e2e": {"value": round(val, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
