@@ -63,3 +63,14 @@ def test_per_iteration_report_compressed_payloads():
         assert d["modes"] == {"compressed": 16}
         assert 0.05 < d["changed_fraction"] < 0.15
         assert abs(d["wire_bytes_per_value"] - (1.0 + d["changed_fraction"])) < 0.01
+
+
+def test_per_iteration_report_rans_payloads():
+    """The RANS sender's histograms are part of the restored state: every
+    repetition codes with the same table and rebuilds exactly."""
+    lines = _bench("--per-iteration", "--config", "2", "--variant", "experts4", "--reps", "2",
+                   "--sender", "rans")
+    assert len(lines) == 9
+    for d in lines:
+        assert d["modes"] == {"rans": 16} and d["raw_ahead"] is None
+        assert 1.2 < d["wire_bytes_per_value"] < 1.5
