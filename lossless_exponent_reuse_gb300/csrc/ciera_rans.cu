@@ -324,6 +324,48 @@ __device__ __forceinline__ void stream_group(int gi, bool in, const uint4& w0, c
   if (in && lane == __ffs(same) - 1) atomicAdd(&hist[sample], static_cast<uint32_t>(__popc(same)));
 }
 
+// The tile's records, assembled in the exponent region (free once the tile
+// is coded) in their payload order and stored by one bulk copy from thread 0:
+// one warp per changed block writes its record there (word counts, each
+// lane's stream behind them, zero padding), where scattered 2-byte global
+// stores would otherwise carry each lane's stream.  Kept out of line so that
+// the kernel's own code keeps the layout it has without it.  Every thread of
+// the CTA calls it.
+__device__ __noinline__ void store_records_bulk(const CompressParams& p, const RansLayout& Ly,
+                                                int nblk, uint8_t* es, const uint8_t* scr,
+                                                const uint32_t* rsize, const uint32_t* rpre,
+                                                uint32_t X, uint32_t agg, uint8_t* payload,
+                                                int64_t BB, int64_t LW, int warp, int lane,
+                                                int tid) {
+  int i = 0;
+  for (int kb = 0; kb < nblk; ++kb) {
+    if (!rsize[kb]) continue;
+    if (i++ % (kThreads / 32) != warp) continue;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(es + 16 * rpre[kb]);
+    const uint8_t* buf = scr + kb * BB;
+    const uint16_t* head = reinterpret_cast<const uint16_t*>(buf);
+    const uint32_t n = head[lane];
+    const uint32_t pre = head[kRansLanes + lane];
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(buf + kRansBufHead) +
+                          (lane + 1) * LW - n;
+    dst[lane] = static_cast<uint16_t>(n);
+    uint16_t* d = dst + kRansLanes + pre;
+    for (uint32_t k = 0; k < n; ++k) d[k] = src[k];
+    const uint32_t words = kRansLanes + head[2 * kRansLanes];
+    if (words + lane < 8u * rsize[kb]) dst[words + lane] = 0;
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0 && agg > 0) {
+    const int64_t at = Ly.D + 16 * static_cast<int64_t>(X);
+    if (in_bounds(p.ctl, at, 16 * static_cast<int64_t>(agg), p.stride)) {
+      bulk_s2g(payload + at, es, 16u * agg);
+      bulk_commit();
+      bulk_wait_read_all();  // the CTA's shared memory outlives the copy's reads
+    }
+  }
+}
+
 struct RansShared {
   uint32_t ticket;
   uint32_t epoch;  // this launch's tag of look-back and flag words
@@ -490,11 +532,17 @@ __global__ void __launch_bounds__(kThreads)
 
   const int64_t limit = 2 * x.len;  // a payload this large goes out raw instead
   // The tile's records are one contiguous run of 16-byte units at D + 16 X.
-  // One warp per changed block stores its record: lane l writes its word
-  // count and copies its own stream (the top of its region) to its place
-  // behind the counts; the lanes below the padding write its zeros.  Records
-  // that would end past 2*len are not stored: the shard then goes out raw.
-  if (!direct_raw && Ly.D + 16 * (static_cast<int64_t>(sh.X) + sh.agg) <= limit) {
+  // Records that would end past 2*len are not stored: the shard then goes
+  // out raw.  When they fit in the tile's exponent region they are assembled
+  // there and stored in one bulk copy; otherwise one warp per changed block
+  // stores its record: lane l writes its word count and copies its own
+  // stream (the top of its region) to its place behind the counts, and the
+  // lanes below the padding write its zeros.
+  if (!direct_raw && Ly.D + 16 * (static_cast<int64_t>(sh.X) + sh.agg) <= limit &&
+      16 * static_cast<int64_t>(sh.agg) <= static_cast<int64_t>(te)) {
+    store_records_bulk(p, Ly, x.nblk, es, scr, rsize, rpre, sh.X, sh.agg, payload, BB, LW, warp,
+                       lane, tid);
+  } else if (!direct_raw && Ly.D + 16 * (static_cast<int64_t>(sh.X) + sh.agg) <= limit) {
     int i = 0;
     for (int kb = 0; kb < x.nblk; ++kb) {
       if (!rsize[kb]) continue;
