@@ -54,16 +54,22 @@ def parse_args():
                          "3-15 of workload 5, all three of its change rates")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=5)
-    ap.add_argument("--variant", default="")
+    ap.add_argument("--config", type=int, default=5,
+                    help="1 matrix 256x512 (declined by the predicate), 2 OLMoE MoE layer, "
+                         "3 the same layer's warm-up regime, 4 16-layer OLMoE stack, "
+                         "5 fine-grained MoE layer (default)")
+    ap.add_argument("--variant", default="",
+                    help="comma-separated: clustered<p> (each block perturbed with "
+                         "probability p, others untouched), experts<k> (cut to k experts)")
     ap.add_argument("--schedule", choices=["sequential", "pipelined", "graph"],
                     default="sequential",
                     help="sequential: compress then decompress layer by layer (per-kernel "
                          "timing); pipelined: compress(i+1) on a side stream overlapping "
                          "decompress(i); graph: the pipelined step replayed from a CUDA graph")
     ap.add_argument("--sender", choices=["exact", "hash", "rans"], default="exact",
-                    help="change test: exact exponent compare (default) or the 128-bit "
-                         "block hash with a 16-byte-per-block HashCache")
+                    help="exact: exponent compare against the sender cache (default); hash: "
+                         "the 128-bit block hash with a 16-byte-per-block HashCache; rans: "
+                         "the changed blocks' exponents rANS-coded (RANS payloads)")
     ra = ap.add_mutually_exclusive_group()
     ra.add_argument("--raw-ahead", dest="raw_ahead", action="store_true", default=None,
                     help="exact/hash senders: shards whose last payload was RAW skip the "
