@@ -32,9 +32,10 @@
 //                      (flags by the exact test, cache refresh, sign+mantissa
 //                      bytes to their fixed positions, the tile's exponents
 //                      into shared memory, the sampled histogram); one warp
-//                      per changed block codes it; decoupled look-back over
-//                      the record sizes places the records, which one warp
-//                      per block stores lane by lane.
+//                      per changed block codes it; then a decoupled
+//                      look-back over the record sizes places the records,
+//                      assembled in shared memory and stored by one bulk
+//                      copy per tile (lane by lane when they do not fit).
 //   k_rans_raw_fixup   rewrites a shard raw when its RANS payload would not
 //                      have been smaller than the raw bytes.
 //   k_rans_dec_tables  one CTA per RANS rank: a slot -> (symbol, frequency,
@@ -371,6 +372,7 @@ struct RansShared {
   uint32_t epoch;  // this launch's tag of look-back and flag words
   uint32_t X;      // record units (16 bytes) before the tile in its shard
   uint32_t agg;    // record units of the tile
+  uint32_t coded;  // set once the tile's blocks are coded and its aggregate published
 };
 
 __global__ void __launch_bounds__(kThreads)
@@ -406,6 +408,7 @@ __global__ void __launch_bounds__(kThreads)
       atomicExch(&p.ctl->ticket, static_cast<unsigned long long>(launch + 1u) << 32);
     sh.ticket = t;
     sh.epoch = launch % 0xffffffffu + 1u;
+    sh.coded = 0;
     fw[0] = 0;
   }
   if (dynamic_smem_size() < static_cast<uint32_t>(rans_compress_smem(T, B)) || T > 32 ||
@@ -460,8 +463,19 @@ __global__ void __launch_bounds__(kThreads)
   const uint32_t mG = static_cast<uint32_t>(((1ull << 32) + B / 16 - 1) / (B / 16));
   if (warp == 0) {
     bool to = false;
-    const uint32_t X =
-        direct_raw ? 0u : lookback_exclusive(p, x, sh.epoch, lane, x.k0 * (BB / 16), &to);
+    uint32_t X = 0;
+    if (!direct_raw) {
+      // The look-back starts once this tile is coded: its predecessors code
+      // at the same time, so polling earlier finds nothing and takes issue
+      // slots from the coding warps.  The wait is bounded like every other.
+      const uint64_t t0 = globaltimer();
+      while (!*reinterpret_cast<volatile uint32_t*>(&sh.coded)) {
+        if (globaltimer() - t0 > p.timeout_ns) break;
+        __nanosleep(256);
+      }
+      __syncwarp();
+      X = lookback_exclusive(p, x, sh.epoch, lane, x.k0 * (BB / 16), &to);
+    }
     if (lane == 0) {
       sh.X = X;
       if (to) record_status(p.ctl, kStatusTimeout);
@@ -525,6 +539,7 @@ __global__ void __launch_bounds__(kThreads)
       const bool skip = (p.flags & CIERA_DEBUG_SKIP_FIRST_PUBLISH) && x.t == 0;
       if (!direct_raw && !skip)
         publish(p, x, sh.epoch, x.t == 0 ? kStateInclusive : kStateAggregate, run);
+      *reinterpret_cast<volatile uint32_t*>(&sh.coded) = 1u;
     }
   }
   __syncthreads();
